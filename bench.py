@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the DeepSelect top-k library on GB300.
+
+One step = one ds_topk call over one batch of the workload (all rows): the
+random block order, the streaming filter, the in-loop radix selects, the
+split-row merge and the final sort.  The headline workload is the DSA
+index-score batch (64 rows x 32768 bf16, k = 512, B = B2 = 1024); the other
+workloads are reported under "per_config".
+
+Timing: inputs are resident in HBM, rotated over enough replicas that the
+replicas together are at least four times the L2 size, so every step reads
+its batch from DRAM.  The K timed launches are replayed from CUDA graphs and
+bracketed by CUDA events on the launching stream (plus a barrier and a
+device synchronize on both sides).  "e2e" times the host-buffer entry point
+ds_topk_host: pinned host input -> device -> top-k -> pinned host output,
+synchronised every step.
+
+Multi-GPU (torchrun): every rank runs its own full batch (weak scaling, no
+data exchange); rank 0 prints the total rows of all ranks over the slowest
+rank's time.
+
+--impl reference times the CPU oracle (single thread, the plain definition
+by full sort) on the same workload, each step a bounded sample of rows.
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "top-k rows/s and input-read HBM GB/s (fraction of GB300 peak) per config"
+UNIT = "rows/s"
+MAIN = "dsa_index_bf16"
+SEED = 0x5EED5EED
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+KERNEL_SOURCES = [os.path.join(ROOT, "top_selection_deepselect_gb300", "csrc", f)
+                  for f in ("ds_topk.cu", "ds_device.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=MAIN, choices=workloads.CONFIG_ORDER)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip per-config lines, torch.topk and the CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
+    ap.add_argument("--burn-seconds", type=float, default=0.5,
+                    help="extra untimed back-to-back warm-up before the timed region")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def profile_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    if it was taken on the current kernel sources."""
+    path = os.path.join(PROFILE_DIR, "deepselect_topk_kernel__%s.txt" % workload)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, _, v = line.partition(":")
+                fields[k.strip()] = v.strip()
+    if fields.get("source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in a child process (our own PID)."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                for name, v in zip(names, r[5:9]):
+                    if v.strip() == "Active":
+                        reasons.add(name)
+            except (IndexError, ValueError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def cfg_desc(c, name, plan=None):
+    d = {"workload": name, "rows": c["rows"], "N": c["N"], "k": c["k"], "B": c["B"],
+         "B2": c["B2"], "dtype": c["dtype"], "desc": c["desc"]}
+    if plan:
+        d["plan"] = plan
+    return d
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle
+# ---------------------------------------------------------------------------
+def oracle_rows_per_s(name, seconds=None, steps=None, warmup=0, rows_per_step=4):
+    import oracle
+    c = workloads.CONFIGS[name]
+    bits, row_len = workloads.config_inputs(name)
+    rows = c["rows"]
+    step_rows = max(1, min(rows_per_step, rows))
+
+    def one_step(i):
+        r0 = (i * step_rows) % rows
+        sel = [(r0 + j) % rows for j in range(step_rows)]
+        rl = None if row_len is None else row_len[sel]
+        oracle.topk(np.ascontiguousarray(bits[sel]), c["dtype"], c["k"], row_len=rl)
+
+    for i in range(warmup):
+        one_step(i)
+    done = 0
+    t0 = time.perf_counter()
+    if steps is not None:
+        for i in range(steps):
+            one_step(warmup + i)
+        done = steps
+    else:
+        while True:
+            one_step(warmup + done)
+            done += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+    dt = time.perf_counter() - t0
+    return done * step_rows / dt, dt, done, step_rows
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    name = args.workload
+    c = workloads.CONFIGS[name]
+    rate, dt, done, step_rows = oracle_rows_per_s(name, steps=args.steps, warmup=args.warmup)
+    sample = "%d steps x %d rows of %s (rows cycled), single thread" % (done, step_rows, name)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(done, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": c["dtype"], "data": "synthetic (seeded; stands in for DSA index scores)",
+        "config": cfg_desc(c, name),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Workload:
+    """Device-resident replicas of one workload plus the launch closure."""
+
+    def __init__(self, name, dev, torch, ds, l2_bytes, max_bytes=8 << 30):
+        self.name = name
+        self.c = c = workloads.CONFIGS[name]
+        self.torch = torch
+        self.ds = ds
+        bits, row_len = workloads.config_inputs(name)
+        self.bits, self.row_len_np = bits, row_len
+        self.esz = 4 if c["dtype"] == "fp32" else 2
+        self.code = ds.DS_FP32 if c["dtype"] == "fp32" else ds.DS_BF16
+        tdt = torch.float32 if c["dtype"] == "fp32" else torch.bfloat16
+        host = torch.from_numpy(bits.view(np.int32 if c["dtype"] == "fp32" else np.int16))
+        one = host.to(dev).view(tdt)
+        nbytes = one.numel() * self.esz
+        # replicas whose total is >= 4x L2, at most 512 launches per graph
+        self.replicas = int(max(2, min(math.ceil(4 * l2_bytes / nbytes), max_bytes // nbytes, 512)))
+        self.l2_defeated = self.replicas * nbytes >= 4 * l2_bytes
+        self.x = torch.empty((self.replicas,) + tuple(one.shape), dtype=tdt, device=dev)
+        self.x[:] = one
+        self.rl = None if row_len is None else torch.from_numpy(row_len).to(dev)
+        self.out_idx = torch.empty((c["rows"], c["k"]), dtype=torch.int32, device=dev)
+        self.out_val = torch.empty((c["rows"], c["k"]), dtype=tdt, device=dev)
+        self.rows = c["rows"]
+        self.read_bytes = workloads.algorithmic_bytes(name, row_len=row_len)
+        self.plan = ds.ds_topk_plan(self.x.data_ptr(), self.code, c["rows"], c["N"], c["k"],
+                                    c["B"], c["B2"], 0)
+        # one eager call first: attribute set-up and cluster checks happen outside any capture
+        self.launch(0, torch.cuda.current_stream(dev).cuda_stream)
+        torch.cuda.synchronize(dev)
+
+    def launch(self, i, stream_handle):
+        c = self.c
+        lib = self.ds.load_library()
+        import ctypes
+        rc = lib.ds_topk(self.x[i % self.replicas].data_ptr(), self.code, c["rows"],
+                         None if self.rl is None else self.rl.data_ptr(), c["N"], c["k"], c["B"],
+                         c["B2"], ctypes.c_uint64(SEED), self.out_idx.data_ptr(),
+                         self.out_val.data_ptr(), stream_handle)
+        if rc != 0:
+            raise self.ds.DSError(rc, "ds_topk", self.ds.ds_last_error_detail())
+
+
+def capture_graph(torch, wl, n, first):
+    """A CUDA graph of n launches starting at replica index `first`."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        h = torch.cuda.current_stream().cuda_stream
+        for i in range(n):
+            wl.launch(first + i, h)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_steps(torch, wl, steps, warmup, dist=None, burn_seconds=0.5):
+    """Device time of exactly `steps` launches (graph replays), max over ranks."""
+    per_graph = wl.replicas
+    full, rest = divmod(steps, per_graph)
+    g_full = capture_graph(torch, wl, per_graph, 0) if full else None
+    g_rest = capture_graph(torch, wl, rest, 0) if rest else None
+    stream = torch.cuda.current_stream()
+    # warm-up: W launches, then at least ~0.5 s of back-to-back graphs
+    h = stream.cuda_stream
+    for i in range(warmup):
+        wl.launch(i, h)
+    torch.cuda.synchronize()
+    t_end = time.perf_counter() + burn_seconds
+    g_warm = g_full or g_rest
+    while time.perf_counter() < t_end:
+        g_warm.replay()
+        torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(full):
+        g_full.replay()
+    if rest:
+        g_rest.replay()
+    end.record(stream)
+    end.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms
+
+
+def time_e2e(torch, ds, wl, steps):
+    """ds_topk_host from pinned host buffers, synchronised every step."""
+    c = wl.c
+    tdt = wl.x.dtype
+    host_dtype = torch.int32 if c["dtype"] == "fp32" else torch.int16
+    x_host = torch.from_numpy(wl.bits.view(np.int32 if c["dtype"] == "fp32" else np.int16)).pin_memory()
+    rl_host = None if wl.row_len_np is None else torch.from_numpy(wl.row_len_np).pin_memory()
+    oi_host = torch.empty((c["rows"], c["k"]), dtype=torch.int32).pin_memory()
+    ov_host = torch.empty((c["rows"], c["k"]), dtype=host_dtype).pin_memory()
+    x_dev = torch.empty((c["rows"], c["N"]), dtype=tdt, device="cuda")
+    rl_dev = None if rl_host is None else torch.empty(c["rows"], dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def one():
+        ds.ds_topk_host(x_host.data_ptr(), wl.code, c["rows"],
+                        None if rl_host is None else rl_host.data_ptr(), c["N"], c["k"], c["B"],
+                        c["B2"], SEED, oi_host.data_ptr(), ov_host.data_ptr(), x_dev.data_ptr(),
+                        None if rl_dev is None else rl_dev.data_ptr(), wl.out_idx.data_ptr(),
+                        wl.out_val.data_ptr(), stream)
+
+    for _ in range(3):
+        one()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    dt = time.perf_counter() - t0
+    h2d = c["rows"] * c["N"] * wl.esz + (0 if rl_host is None else 4 * c["rows"])
+    d2h = c["rows"] * c["k"] * (4 + wl.esz)
+    return c["rows"] * steps / dt, h2d, d2h
+
+
+def time_torch_topk(torch, wl, steps):
+    """torch.topk(sorted=True) on the same replicas (context only)."""
+    c = wl.c
+    xs = wl.x
+    if wl.rl is not None:  # ragged rows: mask the tails first (not timed)
+        xs = wl.x.clone()
+        cols = torch.arange(c["N"], device=xs.device)[None, :]
+        mask = cols >= wl.rl[:, None]
+        xs[:, mask] = float("-inf")
+    for i in range(3):
+        torch.topk(xs[i % wl.replicas], c["k"], dim=-1, largest=True, sorted=True)
+    torch.cuda.synchronize()
+    n = min(steps, 200)
+    mode = "graph"
+    try:
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            for i in range(min(n, wl.replicas)):
+                torch.topk(xs[i % wl.replicas], c["k"], dim=-1, largest=True, sorted=True)
+        torch.cuda.current_stream().wait_stream(s)
+        reps = max(1, n // min(n, wl.replicas))
+        g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * min(n, wl.replicas))
+    except Exception:
+        mode = "eager"
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(n):
+            torch.topk(xs[i % wl.replicas], c["k"], dim=-1, largest=True, sorted=True)
+        e1.record()
+        e1.synchronize()
+        ms = e0.elapsed_time(e1) / n
+    return {"rows_per_s": c["rows"] / (ms * 1e-3), "us_per_call": ms * 1e3, "timing": mode}
+
+
+def run_ours(args, rank, world):
+    import torch
+    import top_selection_deepselect_gb300 as ds
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+        dist = tdist
+    ds.load_library()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    peak, peak_kind = measured_peaks()
+
+    wl = Workload(args.workload, dev, torch, ds, l2)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    ms = time_steps(torch, wl, args.steps, args.warmup, dist=dist, burn_seconds=args.burn_seconds)
+    clocks = sampler.stop() if sampler else None
+    status = ds.ds_topk_device_status()
+    if status != 0:
+        raise SystemExit("device status %d after the timed region" % status)
+
+    ms_per_step = ms / args.steps
+    value = world * wl.rows * args.steps / (ms * 1e-3)
+    achieved = wl.read_bytes / (ms_per_step * 1e-3) / 1e9
+    c = wl.c
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"],
+        "data": "synthetic (seeded; stands in for DSA index scores)",
+        "config": dict(cfg_desc(c, args.workload, wl.plan),
+                       l2="inputs rotated over %d device replicas (%.0f MB >= 4x L2 %.0f MB)"
+                          % (wl.replicas, wl.replicas * c["rows"] * c["N"] * wl.esz / 1e6,
+                             l2 / 1e6),
+                       parallelism="rows per rank, no exchange" if world > 1 else "1 GPU"),
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": profile_traffic(args.workload),
+                     "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": wl.read_bytes,
+                     "kernel": "deepselect_topk_kernel"},
+        "clocks": clocks,
+    }
+    if rank == 0:
+        e2e_steps = args.e2e_steps or args.steps
+        e2e_rate, h2d, d2h = time_e2e(torch, ds, wl, e2e_steps)
+        line["e2e"] = {"value": e2e_rate * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                       "path": "ds_topk_host (pinned host buffers, synchronised per step)"}
+    if rank == 0 and world == 1 and not args.no_extras:
+        line["torch_topk"] = time_torch_topk(torch, wl, args.steps)
+        per = {}
+        for name in workloads.CONFIG_ORDER:
+            w2 = wl if name == args.workload else Workload(name, dev, torch, ds, l2)
+            ms2 = time_steps(torch, w2, args.steps, args.warmup, burn_seconds=args.burn_seconds)
+            us = 1e3 * ms2 / args.steps
+            gbs = w2.read_bytes / (us * 1e-6) / 1e9
+            per[name] = {"us_per_call": us, "rows_per_s": w2.rows / (us * 1e-6), "gbs": gbs,
+                         "frac_of_measured_hbm": gbs / peak, "l2_defeated": w2.l2_defeated,
+                         "algorithmic_bytes": w2.read_bytes, "plan": w2.plan,
+                         "torch_topk": time_torch_topk(torch, w2, args.steps)}
+            if w2 is not wl:
+                del w2
+                torch.cuda.empty_cache()
+        line["per_config"] = per
+        rate, dt, done, step_rows = oracle_rows_per_s(args.workload, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": "%d rows of %s in %.1f s (rows cycled), single thread"
+                                          % (done * step_rows, args.workload, dt)}
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * ds_topk.h -- C ABI of the GB300 DeepSelect top-k library (libds_topk.so).
+ *
+ * Operation (PFCCLab/DeepSelect "DeepSelect-deep-dive", section "算法", and
+ * milkfeng.top "CUDA 算子笔记 4", section "Top K Selection"): for every row r
+ * of a [rows x N] score matrix, return the k largest of its first row_len[r]
+ * elements and their indices.  The result is exact and unique:
+ *   - order: value descending; NaN (any payload) above +inf; -0.0 == +0.0;
+ *     equal values by lower index first;
+ *   - out_idx[r*k + i] = row-local index (int32) of the i-th element,
+ *     out_val[r*k + i] = its value, bit for bit as it was read (same dtype
+ *     as x);
+ *   - a row with fewer than k valid elements fills the rest with index -1
+ *     and value -inf.
+ * The result does not depend on `seed`, on the split factor or on any other
+ * launch choice; `seed` only fixes the random block order the scan uses
+ * (section "算法": the block order must be random and independent of x), and
+ * with it the amount of selection work and the counters of ds_topk_ex.
+ *
+ * Memory: every pointer passed to ds_topk / ds_topk_ex is device memory owned
+ * by the caller.  The library allocates nothing on the device and keeps no
+ * per-call state; it caches a few attributes per device and reports device
+ * time-outs through a per-device status word (ds_topk_device_status).
+ *
+ * Layout: x is row-major with a row pitch of N elements; row r starts at
+ * element r*N.  Outputs are row-major [rows][k].  Any alignment of x works;
+ * when x is 16-byte aligned and N*sizeof(elem) and B*sizeof(elem) are
+ * multiples of 16 the rows are staged into shared memory by bulk (TMA)
+ * copies, otherwise by plain loads.
+ *
+ * Asynchrony: ds_topk and ds_topk_ex only enqueue work on `stream` (a
+ * cudaStream_t, NULL for the legacy default stream) and return; they never
+ * synchronise the host.  ds_topk_host synchronises before it returns.
+ *
+ * Errors: functions return DS_OK (0) or a negative status; argument errors
+ * are reported before anything is enqueued.  ds_strerror gives a fixed text
+ * per status and ds_last_error_detail a message for the calling thread's
+ * most recent failure.  Device-side conditions that cannot be reported
+ * synchronously: row_len[r] > N is read as N, row_len[r] < 0 as 0.
+ */
+#ifndef DS_TOPK_H
+#define DS_TOPK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS_OK 0
+#define DS_EINVAL (-1)       /* an argument is out of range or a pointer is NULL */
+#define DS_EUNSUPPORTED (-2) /* dtype unknown, or the working set does not fit in shared memory */
+#define DS_ECUDA (-3)        /* a CUDA runtime call failed (see ds_last_error_detail) */
+#define DS_EDEVICE (-4)      /* a kernel gave up waiting for a copy (device status word set) */
+
+#define DS_FP32 0
+#define DS_BF16 1
+
+/* Launch plan chosen for a call (filled by ds_topk_plan). */
+typedef struct {
+    int splits;           /* CTAs cooperating on one row (thread-block cluster size) */
+    int threads;          /* threads per CTA */
+    int stages;           /* shared-memory ring depth, in stages */
+    int blocks_per_stage; /* B-blocks staged per ring stage */
+    int warps_per_block;  /* warps filtering one B-block */
+    int bulk;             /* 1: bulk (TMA) copies into shared memory; 0: plain loads */
+    int smem_bytes;       /* dynamic shared memory per CTA */
+    int capacity;         /* candidate-buffer capacity in entries (>= k + B + B2) */
+    int grid;             /* CTAs launched (rows * splits) */
+    int ctas_per_sm;      /* resident CTAs per SM for this plan */
+} ds_plan_t;
+
+/*
+ * ds_topk -- top-k of every row, sorted by (value desc, index asc).
+ *   x        device, [rows][N] elements of `dtype` (DS_FP32 or DS_BF16)
+ *   rows     >= 0 (0 is a no-op)
+ *   row_len  device int32[rows] valid lengths, or NULL for N in every row
+ *   N        row pitch and maximum length, 1 <= N < 2^31
+ *   k        1 <= k <= N
+ *   B, B2    block size and compaction slack of the scan, both >= 1
+ *            (section "算法": compaction runs when the buffer reaches k + B2)
+ *   seed     key of the random block order
+ *   out_idx  device int32[rows][k]
+ *   out_val  device [rows][k] elements of `dtype`
+ *   stream   cudaStream_t or NULL
+ * The split factor is chosen automatically.
+ */
+int ds_topk(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int k, int B,
+            int B2, uint64_t seed, int32_t *out_idx, void *out_val, void *stream);
+
+/*
+ * ds_topk_ex -- ds_topk with an explicit split factor and optional counters.
+ *   splits   0: automatic; 1: one CTA per row; 2..16: the m = ceil(len/B)
+ *            blocks of a row are cut into `splits` contiguous slices of
+ *            ceil(m/splits) blocks, one CTA of a thread-block cluster scans
+ *            each slice and CTA 0 selects the top k of the union
+ *            (section "实现", last paragraph)
+ *   stats    device int64[rows][splits][4] or NULL; when given, every slice
+ *            writes {A, R, W, peak}: elements appended to the candidate
+ *            buffer, compactions inside the loop, total input length of all
+ *            selection calls including the final one, and the largest buffer
+ *            length reached (section "RadixSelectTopK 总处理元素数的期望上界").
+ *            Requires an explicit splits >= 1.
+ */
+int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int k,
+               int B, int B2, uint64_t seed, int splits, int32_t *out_idx, void *out_val,
+               int64_t *stats, void *stream);
+
+/*
+ * ds_topk_host -- the same operation on HOST buffers.
+ *   x_host, row_len_host (nullable), out_idx_host, out_val_host: host memory
+ *   (page-locked memory gives asynchronous copies; pageable memory works).
+ *   x_dev, row_len_dev (NULL iff row_len_host is NULL), out_idx_dev,
+ *   out_val_dev: caller-owned device staging buffers of the same sizes.
+ * Enqueues the host->device copies, the selection and the device->host
+ * copies on `stream`, then synchronises the stream and returns.
+ */
+int ds_topk_host(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
+                 int k, int B, int B2, uint64_t seed, int32_t *out_idx_host, void *out_val_host,
+                 void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev, void *out_val_dev,
+                 void *stream);
+
+/*
+ * ds_topk_plan -- the launch plan ds_topk_ex would use on the current device
+ * (x is only inspected for its alignment).  splits as in ds_topk_ex.
+ */
+int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits,
+                 ds_plan_t *plan);
+
+/* Largest k that fits one CTA's shared memory for this dtype, B and B2 on
+ * the current device (N taken as large as the block order allows), or a
+ * negative status. */
+int ds_topk_max_k(int dtype, int B, int B2);
+
+/* Reads and clears the current device's status word: DS_OK, or DS_EDEVICE if
+ * a kernel gave up waiting for a bulk copy since the last read.
+ * Synchronises the device. */
+int ds_topk_device_status(void);
+
+/* Fixed description of a status code. */
+const char *ds_strerror(int status);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char *ds_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS_TOPK_H */
