@@ -212,13 +212,13 @@ def test_misaligned_input_pointer(dtype):
 
 
 def test_largest_k_that_fits():
+    # ds_topk_max_k assumes the longest row the block order allows: N = 4096 B
     kmax = ds.ds_topk_max_k(ds.DS_FP32, 1024, 1024)
     assert kmax > 2048
-    N = 1 << 16
-    k = min(kmax, N)
-    bits, _ = workloads.generate(2, N, "fp32", "normal", seed=5)
-    ref_idx, ref_val = oracle.topk(bits, "fp32", k)
-    idx, val = run(bits, "fp32", k, 1024, 1024, splits=1)
+    N = 1024 * 4096
+    bits, _ = workloads.generate(1, N, "fp32", "normal", seed=5)
+    ref_idx, ref_val = oracle.topk(bits, "fp32", kmax)
+    idx, val = run(bits, "fp32", kmax, 1024, 1024, splits=1)
     assert_same(idx, val, ref_idx, ref_val)
     with pytest.raises(ds.DSError) as e:
         run(bits, "fp32", kmax + 1, 1024, 1024, splits=1)

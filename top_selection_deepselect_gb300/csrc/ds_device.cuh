@@ -268,7 +268,7 @@ __device__ __forceinline__ uint32_t warp_sum(uint32_t v)
     return v;
 }
 
-__device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
+__device__ __forceinline__ unsigned long long warp_min_reduce(unsigned long long v)
 {
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) {
@@ -281,17 +281,153 @@ __device__ __forceinline__ unsigned long long warp_min_u64(unsigned long long v)
 __device__ __forceinline__ uint32_t lanemask_lt(int lane) { return (1u << lane) - 1u; }
 
 // ---------------------------------------------------------------------------
-// Bitonic sort of P (a power of two) 64-bit entries in shared memory by the
-// whole CTA.  The caller synchronises before; the sort ends synchronised.
+// 64-bit warp helpers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void bitonic_sort_u64(unsigned long long *a, int P, bool descending)
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m)
+{
+    const uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, m);
+    const uint32_t hi = __shfl_xor_sync(kFull, (uint32_t)(v >> 32), m);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_or_u64(unsigned long long v)
+{
+    const uint32_t lo = __reduce_or_sync(kFull, (uint32_t)v);
+    const uint32_t hi = __reduce_or_sync(kFull, (uint32_t)(v >> 32));
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long warp_and_u64(unsigned long long v)
+{
+    const uint32_t lo = __reduce_and_sync(kFull, (uint32_t)v);
+    const uint32_t hi = __reduce_and_sync(kFull, (uint32_t)(v >> 32));
+    return ((unsigned long long)hi << 32) | lo;
+}
+
+__device__ __forceinline__ unsigned long long min_u64(unsigned long long a, unsigned long long b)
+{
+    return a < b ? a : b;
+}
+
+__device__ __forceinline__ unsigned long long max_u64(unsigned long long a, unsigned long long b)
+{
+    return a > b ? a : b;
+}
+
+__host__ __device__ __forceinline__ int pow2_ceil(int v)
+{
+    int p = 1;
+    while (p < v)
+        p <<= 1;
+    return p;
+}
+
+// ---------------------------------------------------------------------------
+// Ordering the selected entries.  A sort network of k entries needs
+// O(log^2 k) dependent steps; here the final position of every entry is its
+// rank -- the number of entries that come before it -- computed with few
+// dependent steps:
+//   * up to 256 entries: every thread counts the entries above its own one;
+//   * up to 2048: each warp sorts a run of 32E entries held in registers
+//     (bitonic, shuffles for strides below 32, register swaps above), then
+//     every entry's rank is its place in its own run plus, for each other
+//     run, the number of entries above it found by binary search.
+// Entries must be distinct; padding entries (0 when descending) never count.
+// ---------------------------------------------------------------------------
+
+// Sorts the 32E entries of one warp's run in registers (all lanes call).
+template <int E>
+__device__ __forceinline__ void warp_bitonic_regs(unsigned long long (&r)[E], int lane, bool desc)
+{
+    constexpr int span = 32 * E;
+#pragma unroll
+    for (int size = 2; size <= span; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int q = stride / 32;
+                    if ((j & q) == 0) {
+                        const int i = 32 * j + lane;
+                        const bool up = ((i & size) == 0) != desc;
+                        const unsigned long long x = r[j], y = r[j + q];
+                        if (up ? (x > y) : (x < y)) {
+                            r[j] = y;
+                            r[j + q] = x;
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const int i = 32 * j + lane;
+                    const unsigned long long o = shfl_xor_u64(r[j], stride);
+                    const bool up = ((i & size) == 0) != desc;
+                    const bool lower = (lane & stride) == 0;
+                    r[j] = (lower == up) ? min_u64(r[j], o) : max_u64(r[j], o);
+                }
+            }
+        }
+    }
+}
+
+// Ranks (descending order: number of entries greater) of the cnt distinct
+// entries a[0, cnt), 256 < cnt <= 32*E*8.  a is padded with zeros to 256E
+// entries by the caller and synchronised.  Each thread gets the entries
+// a[base + 32j + lane] of its warp's run after the call (returned through
+// `vals`) together with their ranks; entries at positions >= cnt are pads.
+// On return a[] holds the warp-sorted runs and the CTA is synchronised.
+template <int E>
+__device__ __forceinline__ void rank_desc_runs(unsigned long long *a, unsigned long long (&vals)[E],
+                                               int (&ranks)[E])
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    constexpr int span = 32 * E;
+    const int base = warp * span;
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+        vals[j] = a[base + 32 * j + lane];
+    warp_bitonic_regs<E>(vals, lane, true);
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+        a[base + 32 * j + lane] = vals[j];
+    __syncthreads();
+    // branch-free binary searches, the eight runs in lockstep so that the
+    // loads of one step are independent: pos[w] = entries of run w above e
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+        const unsigned long long e = vals[j];
+        int pos[kWarps];
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w)
+            pos[w] = 0;
+#pragma unroll
+        for (int step = span / 2; step >= 1; step >>= 1) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                pos[w] += a[w * span + pos[w] + step - 1] > e ? step : 0;
+        }
+        int rank = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const int q = pos[w] + (a[w * span + pos[w]] > e ? 1 : 0);
+            rank += (w == warp) ? (32 * j + lane) : q;
+        }
+        ranks[j] = rank;
+    }
+    __syncthreads();
+}
+
+// Plain shared-memory bitonic sort (any power of two); ends synchronised.
+__device__ __forceinline__ void bitonic_sort_smem(unsigned long long *a, int P, bool desc)
 {
     for (int size = 2; size <= P; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             for (int t = threadIdx.x; t < (P >> 1); t += kThreads) {
                 const int lo = 2 * t - (t & (stride - 1));
                 const int hi = lo + stride;
-                const bool pair_desc = (((lo & size) == 0) == descending);
+                const bool pair_desc = (((lo & size) == 0) == desc);
                 const unsigned long long x = a[lo], y = a[hi];
                 if (pair_desc ? (x < y) : (x > y)) {
                     a[lo] = y;
@@ -303,162 +439,354 @@ __device__ __forceinline__ void bitonic_sort_u64(unsigned long long *a, int P, b
     }
 }
 
-__host__ __device__ __forceinline__ int pow2_ceil(int v)
+// Sorts the cnt distinct entries a[0, cnt) ascending, in place (block
+// order); positions past cnt are left as they are.  Caller synchronises
+// before; ends synchronised.
+__device__ __forceinline__ void sort_asc_small(unsigned long long *a, int cnt, int cap_pow2)
 {
-    int p = 1;
-    while (p < v)
-        p <<= 1;
-    return p;
+    if (cnt <= kThreads) {
+        const int t = threadIdx.x;
+        unsigned long long e = 0ull;
+        int rank = 0;
+        if (t < cnt) {
+            e = a[t];
+            for (int j = 0; j < cnt; ++j)
+                rank += a[j] < e ? 1 : 0;
+        }
+        __syncthreads();
+        if (t < cnt)
+            a[rank] = e;
+        __syncthreads();
+    } else {
+        for (int i = cnt + threadIdx.x; i < cap_pow2; i += kThreads)
+            a[i] = ~0ull;
+        __syncthreads();
+        bitonic_sort_smem(a, cap_pow2, false);
+    }
 }
 
-// Scratch words of one CTA's radix select and stage decisions.
+// Shared scratch words of one CTA.
 struct Misc {
     unsigned long long bar[kMaxStages];  // one mbarrier per ring stage
-    unsigned long long tmin;             // smallest selected composite
-    int cntw[kWarps];                    // survivors per warp in the current stage
+    unsigned long long wor[kWarps];      // per-warp OR / AND / min of composites
+    unsigned long long wand[kWarps];
+    unsigned long long wmin[kWarps];
+    unsigned long long group[32];        // small tie group of the select
+    unsigned long long texact;           // exact k-th composite, when resolved
+    __align__(16) int cntw[2][kWarps];   // survivors per warp, double-buffered
+    uint32_t wsum[kWarps];               // per-warp totals of block scans
     uint32_t sel_digit, sel_above, sel_eq;
-    int hole_count, mover_count;
+    int group_count;
     int flag;                            // a wait timed out
-    int merge_count[kMaxSplits];         // partial-result sizes (CTA 0 of a cluster)
+    int merge_count;                     // CTA 0 of a cluster: entries received
+    int merge_off;                       // this CTA's offset in CTA 0's merge buffer
 };
 
-// ---------------------------------------------------------------------------
-// RadixSelectTopK ("算法", step 3) on n > k composites in shared memory.
-//
-// Digits of 8 bits are taken from the most significant end: first the order
-// key (4 digits for fp32, 2 for bf16), then the complemented index (only its
-// low idx_bits bits vary).  Each pass builds a 256-bin histogram of the
-// entries that still match the selected prefix, with warp-aggregated shared
-// atomics (one atomic per distinct digit per warp), and one warp scans the
-// bins from the top to find the digit holding the k-th entry.  The loop stops
-// as soon as every entry matching the prefix is needed, so distinct keys
-// rarely reach the index digits.
-//
-// Afterwards the k selected entries -- (c & pmask) >= prefix -- are moved to
-// cand[0, k) in place: unselected slots below k are listed, selected entries
-// at or above k are moved into them.  Returns the smallest selected
-// composite, the new threshold.  Called by all threads; ends synchronised.
-// ---------------------------------------------------------------------------
-template <int DT>
-__device__ unsigned long long radix_select_topk(unsigned long long *cand, int n, int k,
-                                                uint32_t *hist /* 2 x 256 */,
-                                                uint16_t *holes, Misc *ms, int idx_bits)
+// Exclusive scan of one value per thread over the CTA (thread order).
+// Uses ms->wsum; ends synchronised.  Returns the exclusive prefix.
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, Misc *ms)
 {
-    using E = Elem<DT>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_inclusive_scan(v, lane);
+    if (lane == 31)
+        ms->wsum[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        before += (w < warp) ? ms->wsum[w] : 0u;
+    return before + incl - v;
+}
+
+// ---------------------------------------------------------------------------
+// RadixSelectTopK ("算法", step 3) on n > k distinct composites in shared
+// memory.  After the call cand[0, k) holds the k largest (in no particular
+// order); returns the smallest of them, the new threshold.  Called by all
+// threads; ends synchronised.
+//
+// Every thread loads its entries cand[tid + 256j] into registers once (up to
+// R of them); all passes then work on registers:
+//  1. OR and AND of all composites: only bits where they differ can separate
+//     entries, so digits start at the highest such bit and skip bits that
+//     never vary.
+//  2. Digit passes of 8 bits from the top: each warp builds its own 256-bin
+//     histogram of the entries still matching the chosen prefix with shared
+//     atomics (warps never contend); the CTA sums the eight histograms, scans
+//     them from the top bin down and picks the digit that holds the k-th
+//     entry.
+//  3. The loop stops when every entry matching the prefix is needed, or when
+//     at most 32 remain tied, which one warp ranks directly to find the exact
+//     k-th composite.
+//  4. Compaction: a CTA-wide scan of per-thread selected counts gives every
+//     selected entry its slot in cand[0, k); all entries are in registers, so
+//     the buffer is overwritten in place.
+// ---------------------------------------------------------------------------
+template <int R>
+static __device__ __noinline__ unsigned long long radix_select_regs(unsigned long long *cand, int n,
+                                                                    int k, uint32_t *whist,
+                                                                    Misc *ms)
+{
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long v[R];
+    uint32_t valid = 0u;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int i = tid + kThreads * j;
+        v[j] = 0ull;
+        if (i < n) {
+            v[j] = cand[i];
+            valid |= 1u << j;
+        }
+    }
+
+    // 1. varying bits
+    unsigned long long vo = 0ull, va = ~0ull;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if (valid & (1u << j)) {
+            vo |= v[j];
+            va &= v[j];
+        }
+    }
+    vo = warp_or_u64(vo);
+    va = warp_and_u64(va);
+    if (lane == 0) {
+        ms->wor[warp] = vo;
+        ms->wand[warp] = va;
+    }
+    if (tid == 0)
+        ms->group_count = 0;
+    __syncthreads();
+    vo = 0ull;
+    va = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        vo |= ms->wor[w];
+        va &= ms->wand[w];
+    }
+    const unsigned long long vary = vo ^ va;
+
+    // 2./3. digit passes
+    unsigned long long prefix = 0ull, pmask = 0ull, texact = 0ull;
+    bool exact = false;
+    uint32_t need = (uint32_t)k;
+    uint32_t live = valid;  // entries still matching the prefix
+    int h = 63 - __clzll((long long)vary);
+    uint32_t *wh = whist + warp * 256;
+    while (true) {
+        const int lo = h >= 7 ? h - 7 : 0;
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if (live & (1u << j))
+                atomicAdd(&wh[(uint32_t)(v[j] >> lo) & 255u], 1u);
+        __syncthreads();
+        // thread t owns bin 255 - t: scanning in thread order walks the bins
+        // from the top down
+        const int bin = 255 - tid;
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            cnt += whist[w * 256 + bin];
+            whist[w * 256 + bin] = 0u;
+        }
+        const uint32_t excl = block_exclusive_scan(cnt, ms);
+        if (excl < need && need <= excl + cnt) {
+            ms->sel_digit = (uint32_t)bin;
+            ms->sel_above = excl;
+            ms->sel_eq = cnt;
+        }
+        __syncthreads();
+        const uint32_t dsel = ms->sel_digit, eq = ms->sel_eq;
+        need -= ms->sel_above;
+        prefix |= (unsigned long long)dsel << lo;
+        pmask |= 255ull << lo;
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if ((live & (1u << j)) && (((uint32_t)(v[j] >> lo) & 255u) != dsel))
+                live &= ~(1u << j);
+        if (eq == need)
+            break;
+        if (eq <= 32u) {
+            // rank the tied entries directly
+            uint32_t mine = (uint32_t)__popc(live);
+            const uint32_t wcount = __reduce_add_sync(kFull, mine);
+            int wbase = 0;
+            if (lane == 0 && wcount)
+                wbase = atomicAdd(&ms->group_count, (int)wcount);
+            wbase = __shfl_sync(kFull, wbase, 0);
+            int off = wbase + (int)(warp_inclusive_scan(mine, lane) - mine);
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+                if (live & (1u << j))
+                    ms->group[off++] = v[j];
+            __syncthreads();
+            if (warp == 0) {
+                const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
+                uint32_t rank = 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const unsigned long long o = shfl_xor_u64(g, j) ;
+                    rank += (((lane ^ j) < (int)eq) && o > g) ? 1u : 0u;
+                }
+                if (lane < (int)eq && rank == need - 1u)
+                    ms->texact = g;
+            }
+            __syncthreads();
+            texact = ms->texact;
+            exact = true;
+            break;
+        }
+        // eq > need >= 1 and composites are distinct: lower bits still vary
+        const unsigned long long below = lo > 0 ? (vary & ((1ull << lo) - 1ull)) : 0ull;
+        if (below == 0ull)
+            break;  // unreachable for distinct composites; keeps the loop finite
+        h = 63 - __clzll((long long)below);
+    }
+
+    // 4. compaction
+    uint32_t sel = 0u;
+    unsigned long long mn = ~0ull;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if (valid & (1u << j)) {
+            const bool s = exact ? (v[j] >= texact) : ((v[j] & pmask) >= prefix);
+            if (s) {
+                sel |= 1u << j;
+                mn = min_u64(mn, v[j]);
+            }
+        }
+    }
+    mn = warp_min_reduce(mn);
+    if (lane == 0)
+        ms->wmin[warp] = mn;
+    uint32_t pos = block_exclusive_scan((uint32_t)__popc(sel), ms);  // all loads are done
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+        if (sel & (1u << j))
+            cand[pos++] = v[j];
+    __syncthreads();
+    if (exact)
+        return texact;
+    unsigned long long t = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        t = min_u64(t, ms->wmin[w]);
+    return t;
+}
+
+// The same for sets too large for registers: every pass reads shared memory.
+static __device__ __noinline__ unsigned long long radix_select_smem(unsigned long long *cand, int n,
+                                                                    int k, uint32_t *whist,
+                                                                    uint16_t *holes, Misc *ms)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    unsigned long long vo = 0ull, va = ~0ull;
+    for (int i = tid; i < n; i += kThreads) {
+        const unsigned long long c = cand[i];
+        vo |= c;
+        va &= c;
+    }
+    vo = warp_or_u64(vo);
+    va = warp_and_u64(va);
+    if (lane == 0) {
+        ms->wor[warp] = vo;
+        ms->wand[warp] = va;
+    }
+    __syncthreads();
+    vo = 0ull;
+    va = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        vo |= ms->wor[w];
+        va &= ms->wand[w];
+    }
+    const unsigned long long vary = vo ^ va;
     unsigned long long prefix = 0ull, pmask = 0ull;
     uint32_t need = (uint32_t)k;
-
-    hist[tid] = 0u;  // kThreads == 256 bins
-    if (tid == 0) {
-        ms->hole_count = 0;
-        ms->mover_count = 0;
-        ms->tmin = ~0ull;
-    }
-    __syncthreads();
-
-    const int ndigits = E::kKeyDigits + idx_bits / 8;
-    for (int d = 0; d < ndigits; ++d) {
-        const int sh = d < E::kKeyDigits ? E::kKeyTopShift - 8 * d
-                                         : idx_bits - 8 - 8 * (d - E::kKeyDigits);
-        uint32_t *h = hist + (d & 1) * 256;
-        for (int base = 0; base < n; base += kThreads) {
-            const int i = base + tid;
-            uint32_t dig = 256u;  // not counted
-            if (i < n) {
-                const unsigned long long c = cand[i];
-                if ((c & pmask) == prefix)
-                    dig = (uint32_t)(c >> sh) & 255u;
-            }
-            const uint32_t peers = __match_any_sync(kFull, dig);
-            if (dig < 256u && lane == __ffs(peers) - 1)
-                atomicAdd(&h[dig], (uint32_t)__popc(peers));
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // lane l owns bins 255-8l down to 248-8l; scan in descending bin order
-            uint32_t c8[8], s = 0;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                c8[t] = h[255 - 8 * lane - t];
-                s += c8[t];
-            }
-            const uint32_t incl = warp_inclusive_scan(s, lane);
-            uint32_t cum = incl - s;
-            if (cum < need && need <= incl) {
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (cum + c8[t] >= need) {
-                        ms->sel_digit = (uint32_t)(255 - 8 * lane - t);
-                        ms->sel_above = cum;
-                        ms->sel_eq = c8[t];
-                        break;
-                    }
-                    cum += c8[t];
-                }
-            }
-        } else {
-            uint32_t *next = hist + ((d + 1) & 1) * 256;
-            for (int b = tid - 32; b < 256; b += kThreads - 32)
-                next[b] = 0u;
-        }
-        __syncthreads();
-        const uint32_t dsel = ms->sel_digit;
-        need -= ms->sel_above;
-        prefix |= (unsigned long long)dsel << sh;
-        pmask |= 255ull << sh;
-        if (ms->sel_eq == need)
-            break;
-    }
-
-    // in-place compaction of the selected entries into cand[0, k)
-    unsigned long long my_min = ~0ull;
-    for (int base = 0; base < k; base += kThreads) {
-        const int i = base + tid;
-        bool hole = false;
-        if (i < k) {
+    int h = 63 - __clzll((long long)vary);
+    uint32_t *wh = whist + warp * 256;
+    while (true) {
+        const int lo = h >= 7 ? h - 7 : 0;
+        for (int i = tid; i < n; i += kThreads) {
             const unsigned long long c = cand[i];
-            if ((c & pmask) >= prefix)
-                my_min = c < my_min ? c : my_min;
-            else
-                hole = true;
+            if ((c & pmask) == prefix)
+                atomicAdd(&wh[(uint32_t)(c >> lo) & 255u], 1u);
         }
-        const uint32_t b = __ballot_sync(kFull, hole);
-        if (b) {
-            int off = 0;
-            if (lane == 0)
-                off = atomicAdd(&ms->hole_count, __popc(b));
-            off = __shfl_sync(kFull, off, 0);
-            if (hole)
-                holes[off + __popc(b & lanemask_lt(lane))] = (uint16_t)i;
+        __syncthreads();
+        const int bin = 255 - tid;
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            cnt += whist[w * 256 + bin];
+            whist[w * 256 + bin] = 0u;
         }
+        const uint32_t excl = block_exclusive_scan(cnt, ms);
+        if (excl < need && need <= excl + cnt) {
+            ms->sel_digit = (uint32_t)bin;
+            ms->sel_above = excl;
+            ms->sel_eq = cnt;
+        }
+        __syncthreads();
+        const uint32_t dsel = ms->sel_digit, eq = ms->sel_eq;
+        need -= ms->sel_above;
+        prefix |= (unsigned long long)dsel << lo;
+        pmask |= 255ull << lo;
+        if (eq == need)
+            break;
+        const unsigned long long below = lo > 0 ? (vary & ((1ull << lo) - 1ull)) : 0ull;
+        if (below == 0ull)
+            break;  // unreachable for distinct composites; keeps the loop finite
+        h = 63 - __clzll((long long)below);
     }
-    __syncthreads();
-    for (int base = k; base < n; base += kThreads) {
-        const int i = base + tid;
-        bool mover = false;
-        unsigned long long c = 0ull;
-        if (i < n) {
-            c = cand[i];
-            mover = (c & pmask) >= prefix;
-            if (mover)
-                my_min = c < my_min ? c : my_min;
-        }
-        const uint32_t b = __ballot_sync(kFull, mover);
-        if (b) {
-            int off = 0;
-            if (lane == 0)
-                off = atomicAdd(&ms->mover_count, __popc(b));
-            off = __shfl_sync(kFull, off, 0);
-            if (mover)
-                cand[holes[off + __popc(b & lanemask_lt(lane))]] = c;
-        }
+    // in-place compaction: unselected slots below k are listed, selected
+    // entries at or above k move into them
+    uint32_t nh = 0, nm = 0;
+    unsigned long long mn = ~0ull;
+    for (int i = tid; i < n; i += kThreads) {
+        const unsigned long long c = cand[i];
+        const bool sel = (c & pmask) >= prefix;
+        if (sel)
+            mn = min_u64(mn, c);
+        if (i < k)
+            nh += sel ? 0u : 1u;
+        else
+            nm += sel ? 1u : 0u;
     }
-    my_min = warp_min_u64(my_min);
+    mn = warp_min_reduce(mn);
     if (lane == 0)
-        atomicMin(&ms->tmin, my_min);
+        ms->wmin[warp] = mn;
+    const uint32_t off = block_exclusive_scan(nh | (nm << 16), ms);
+    uint32_t oh = off & 0xFFFFu, om = off >> 16;
+    for (int i = tid; i < k; i += kThreads)
+        if (!((cand[i] & pmask) >= prefix))
+            holes[oh++] = (uint16_t)i;
     __syncthreads();
-    return ms->tmin;
+    for (int i = tid + kThreads * (k / kThreads); i < n; i += kThreads) {
+        if (i < k)
+            continue;
+        const unsigned long long c = cand[i];
+        if ((c & pmask) >= prefix)
+            cand[holes[om++]] = c;
+    }
+    __syncthreads();
+    unsigned long long t = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        t = min_u64(t, ms->wmin[w]);
+    return t;
+}
+
+__device__ __forceinline__ unsigned long long radix_select_topk(unsigned long long *cand, int n, int k,
+                                                                uint32_t *whist, uint16_t *holes,
+                                                                Misc *ms)
+{
+    if (n <= 8 * kThreads)
+        return radix_select_regs<8>(cand, n, k, whist, ms);
+    if (n <= 12 * kThreads)
+        return radix_select_regs<12>(cand, n, k, whist, ms);
+    if (n <= 24 * kThreads)
+        return radix_select_regs<24>(cand, n, k, whist, ms);
+    return radix_select_smem(cand, n, k, whist, holes, ms);
 }
 
 }  // namespace ds

@@ -1,0 +1,602 @@
+// ds_kernel.cuh -- the DeepSelect top-k kernel for sm_103a (device code).
+//
+// One CTA (256 threads) scans one row, or one slice of a row when the row is
+// split across the CTAs of a thread-block cluster.  The loop is the one of
+// PFCCLab/DeepSelect "DeepSelect-deep-dive", section "算法":
+//   * the row's B-blocks are visited in a random order drawn from Philox
+//     (independent of the data), each one read from HBM exactly once;
+//   * every element above the running threshold T is appended to a
+//     candidate buffer in shared memory;
+//   * after a block, if the buffer holds k + B2 or more entries, a radix
+//     select shrinks it to k and T becomes the smallest kept element.
+// GB300 mapping:
+//   * blocks are staged into a ring of shared-memory stages by bulk (TMA)
+//     copies issued by the lanes of one warp, completion tracked by mbarriers, several
+//     stages ahead of the filter;
+//   * a stage holds one B-block per `warps_per_block` warps; each warp filters
+//     its part with one unordered compare per element (fp32 FSETP, bf16 packed
+//     set.geu); only chunks that may hold a survivor get exact bit masks,
+//     which are walked with __ffs and placed by ballot rank (section "实现":
+//     one-pass mask + __ffs placement);
+//   * the blocks of a stage are filtered in parallel against the same T; a
+//     stage is cut at the first block after which the buffer would reach
+//     k + B2, the buffer is compacted, and the rest of the stage is filtered
+//     again with the new T -- exactly the block-by-block semantics, so the
+//     counters A, R, W and the peak length equal the step-by-step model's;
+//   * split rows (section "实现", last paragraph): each CTA of the cluster
+//     selects the top k of its contiguous slice and stores it into CTA 0's
+//     shared memory (distributed shared memory), CTA 0 selects and orders.
+#pragma once
+
+#include <cooperative_groups.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ds_device.cuh"
+
+namespace cg = cooperative_groups;
+
+namespace ds {
+
+struct Params {
+    const void *x;
+    const int32_t *row_len;
+    int32_t *out_idx;
+    void *out_val;
+    long long *stats;     // counters {A, R, W, peak} per (row, slice), or null
+    unsigned int *status; // device status word: bit 0 = a wait timed out
+    long long N;
+    int k, B, B2;
+    uint32_t seed_lo, seed_hi;
+    int splits;          // CTAs per row
+    int wpb;             // warps per B-block
+    int bps;             // B-blocks per stage (kWarps / wpb)
+    int stages;          // ring depth (1 for the plain-load path)
+    int slot_bytes;      // bytes of one staged block (B * size rounded up to 16)
+    int cpw;             // 16-byte chunks per warp of a block
+    int off_cand, off_perm, off_hist, off_holes, off_misc;
+};
+
+// ---------------------------------------------------------------------------
+// Filter of one warp's part of a block.
+// ---------------------------------------------------------------------------
+struct BlockView {
+    const unsigned char *slot;  // shared-memory copy of the block
+    int lo, hi;                 // row-local element range [lo, hi)
+    int c0, c1;                 // this warp's 16-byte chunks [c0, c1)
+    uint32_t t;                 // prefilter operand
+    bool refine;                // resolve survivors exactly by composite
+    bool plain;                 // no refinement and no partial chunk
+};
+
+// Prefilter bits of one 16-byte chunk, bit e = element e: !(v < t).
+// bf16: the packed unordered compare gives 0xFFFF per passing half; prmt
+// gathers one byte per element and dp4a folds four 0/1 bytes into four bits
+// (section "实现": set.bf16x2 / prmt / dp4a mask generation).
+template <int DT>
+__device__ __forceinline__ uint32_t prefilter_bits(const uint4 v, uint32_t t)
+{
+    if (DT == 0) {
+        const float tf = __uint_as_float(t);
+        return (uint32_t)!(__uint_as_float(v.x) < tf) | ((uint32_t)!(__uint_as_float(v.y) < tf) << 1) |
+               ((uint32_t)!(__uint_as_float(v.z) < tf) << 2) |
+               ((uint32_t)!(__uint_as_float(v.w) < tf) << 3);
+    } else {
+        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+        const uint32_t m0 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.x), t2);
+        const uint32_t m1 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.y), t2);
+        const uint32_t m2 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.z), t2);
+        const uint32_t m3 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.w), t2);
+        const uint32_t lo4 = __byte_perm(m0, m1, 0x7531) & 0x01010101u;
+        const uint32_t hi4 = __byte_perm(m2, m3, 0x7531) & 0x01010101u;
+        return (uint32_t)__dp4a(lo4, 0x08040201u, 0u) | ((uint32_t)__dp4a(hi4, 0x08040201u, 0u) << 4);
+    }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t element_bits(const uint4 v, int e)
+{
+    if (DT == 0) {
+        return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    } else {
+        const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
+        return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
+    }
+}
+
+// Exact survivor mask of chunk c of a block that is not plain: elements past
+// hi are dropped, and with `refine` every candidate is compared as a
+// composite against T.
+template <int DT>
+__device__ __forceinline__ uint32_t chunk_fixup(uint32_t mask, const uint4 v, int c, const BlockView &bv,
+                                                const Threshold &thr)
+{
+    using E = Elem<DT>;
+    const int first = bv.lo + c * E::kPerChunk;
+    const int valid = bv.hi - first;
+    if (valid < E::kPerChunk)
+        mask &= (1u << valid) - 1u;
+    if (bv.refine && mask) {
+        uint32_t m = mask;
+        while (m) {
+            const int e = __ffs(m) - 1;
+            m &= m - 1u;
+            const unsigned long long comp =
+                ((unsigned long long)E::key(element_bits<DT>(v, e)) << 32) |
+                (unsigned long long)(~(uint32_t)(first + e));
+            if (!(comp > thr.comp))
+                mask &= ~(1u << e);
+        }
+    }
+    return mask;
+}
+
+// Exact survivor masks of one lane's chunks, kept in registers: round r
+// (chunk c0 + lane + 32r) occupies kPerChunk bits of the mask words.
+template <int DT, int MAXR>
+struct MaskRegs {
+    static constexpr int kBits = Elem<DT>::kPerChunk;
+    static constexpr int kPerWord = 32 / kBits;
+    static constexpr int kWords = (MAXR + kPerWord - 1) / kPerWord;
+    uint32_t w[kWords];
+    __device__ __forceinline__ uint32_t get(int r) const
+    {
+        return (w[r / kPerWord] >> ((r % kPerWord) * kBits)) & ((1u << kBits) - 1u);
+    }
+};
+
+// NaN-propagating maxima: if any operand is NaN the result is NaN, so
+// !(max < t) holds exactly when !(x < t) holds for some element x.
+__device__ __forceinline__ uint32_t max_nan_f32(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t chunk_max(const uint4 v)
+{
+    if (DT == 0)
+        return max_nan_f32(max_nan_f32(v.x, v.y), max_nan_f32(v.z, v.w));
+    return max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w));
+}
+
+// true if some element summarised by the running maximum m passes !(x < t)
+template <int DT>
+__device__ __forceinline__ bool max_passes(uint32_t m, uint32_t t)
+{
+    if (DT == 0)
+        return !(__uint_as_float(m) < __uint_as_float(t));
+    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
+    return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&m), t2) != 0u;
+}
+
+// Survivors of this warp's chunks.  Fast path: every lane folds its chunks
+// into one NaN-propagating maximum and compares it once (about half an
+// instruction per element); only when some lane passes do the passing lanes
+// build exact per-chunk masks, kept in registers (round r = chunk c0 + lane +
+// 32r, kPerChunk bits each).  Returns the warp's survivor count; lane_cnt is
+// this lane's.
+template <int DT, int MAXR>
+__device__ __forceinline__ int warp_filter(const BlockView &bv, const Threshold &thr, int lane,
+                                           MaskRegs<DT, MAXR> &mk, uint32_t &lane_cnt)
+{
+    using M = MaskRegs<DT, MAXR>;
+    lane_cnt = 0u;
+#pragma unroll
+    for (int i = 0; i < M::kWords; ++i)
+        mk.w[i] = 0u;
+    // the identity of the maximum: -inf (any real element or NaN replaces it)
+    uint32_t mx = DT == 0 ? 0xFF800000u : 0xFF80FF80u;
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r) {
+        const int c = bv.c0 + lane + 32 * r;
+        if (c < bv.c1)
+            mx = DT == 0 ? max_nan_f32(mx, chunk_max<DT>(lds128(bv.slot + c * 16)))
+                         : max_nan_bf16x2(mx, chunk_max<DT>(lds128(bv.slot + c * 16)));
+    }
+    const bool pass = bv.c0 + lane < bv.c1 && max_passes<DT>(mx, bv.t);
+    if (!__any_sync(kFull, pass))
+        return 0;
+    if (pass) {
+#pragma unroll
+        for (int r = 0; r < MAXR; ++r) {
+            const int c = bv.c0 + lane + 32 * r;
+            if (c < bv.c1) {
+                const uint4 v = lds128(bv.slot + c * 16);
+                uint32_t m = prefilter_bits<DT>(v, bv.t);
+                if (!bv.plain)
+                    m = chunk_fixup<DT>(m, v, c, bv, thr);
+                mk.w[r / M::kPerWord] |= m << ((r % M::kPerWord) * M::kBits);
+                lane_cnt += __popc(m);
+            }
+        }
+    }
+    return (int)__reduce_add_sync(kFull, lane_cnt);
+}
+
+// Appends this warp's survivors at cand[base, base + count): one warp scan of
+// the lane counts gives every lane its slot range (predicate / exclusive scan
+// / scatter of "Compact"); each lane walks its masks with __ffs.
+template <int DT, int MAXR>
+__device__ __forceinline__ void warp_append(const BlockView &bv, int lane, const MaskRegs<DT, MAXR> &mk,
+                                            uint32_t lane_cnt, unsigned long long *cand, int base)
+{
+    using E = Elem<DT>;
+    const uint32_t incl = warp_inclusive_scan(lane_cnt, lane);
+    int pos = base + (int)(incl - lane_cnt);
+    if (lane_cnt == 0u)
+        return;
+#pragma unroll
+    for (int r = 0; r < MAXR; ++r) {
+        uint32_t m = mk.get(r);
+        if (m) {
+            const int c = bv.c0 + lane + 32 * r;
+            const uint4 v = lds128(bv.slot + c * 16);
+            const int first = bv.lo + c * E::kPerChunk;
+            do {
+                const int e = __ffs(m) - 1;
+                m &= m - 1u;
+                cand[pos++] = ((unsigned long long)E::key(element_bits<DT>(v, e)) << 32) |
+                              (unsigned long long)(~(uint32_t)(first + e));
+            } while (m);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Final order and output: every selected composite goes straight to its rank
+// in the output row: index = ~low word, value = the bits its key came from
+// (the input is read again only for +-0 and NaN, whose keys do not determine
+// the bits).  Positions past cnt get index -1 and -inf.  Caller synchronises.
+// ---------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void emit(const Params &p, long long obase, int pos,
+                                     unsigned long long c, const unsigned char *xrow)
+{
+    using E = Elem<DT>;
+    const int32_t idx = (int32_t)(~(uint32_t)c);
+    const uint32_t key = (uint32_t)(c >> 32);
+    uint32_t bits;
+    if (key == E::kNanKey || key == E::kZeroKey)
+        bits = DT == 0 ? reinterpret_cast<const uint32_t *>(xrow)[idx]
+                       : reinterpret_cast<const uint16_t *>(xrow)[idx];
+    else
+        bits = E::bits_of_key(key);
+    p.out_idx[obase + pos] = idx;
+    if (DT == 0)
+        reinterpret_cast<uint32_t *>(p.out_val)[obase + pos] = bits;
+    else
+        reinterpret_cast<uint16_t *>(p.out_val)[obase + pos] = (uint16_t)bits;
+}
+
+template <int DT, int E>
+__device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, const Params &p,
+                                          long long obase, const unsigned char *xrow)
+{
+    const int P = 256 * E;
+    for (int i = cnt + threadIdx.x; i < P; i += kThreads)
+        arr[i] = 0ull;
+    __syncthreads();
+    unsigned long long vals[E];
+    int ranks[E];
+    rank_desc_runs<E>(arr, vals, ranks);
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+        if (vals[j] != 0ull)
+            emit<DT>(p, obase, ranks[j], vals[j], xrow);
+}
+
+template <int DT>
+__device__ void sort_and_write(unsigned long long *arr, int cnt, const Params &p, int row,
+                               const unsigned char *xrow)
+{
+    using E = Elem<DT>;
+    const long long obase = (long long)row * p.k;
+    for (int i = cnt + threadIdx.x; i < p.k; i += kThreads) {
+        p.out_idx[obase + i] = -1;
+        if (DT == 0)
+            reinterpret_cast<uint32_t *>(p.out_val)[obase + i] = E::kNegInfBits;
+        else
+            reinterpret_cast<uint16_t *>(p.out_val)[obase + i] = (uint16_t)E::kNegInfBits;
+    }
+    if (cnt <= kThreads) {
+        const int t = threadIdx.x;
+        if (t < cnt) {
+            const unsigned long long e = arr[t];
+            int rank = 0;
+            for (int j = 0; j < cnt; ++j)
+                rank += arr[j] > e ? 1 : 0;
+            emit<DT>(p, obase, rank, e, xrow);
+        }
+    } else if (cnt <= 512) {
+        emit_runs<DT, 2>(arr, cnt, p, obase, xrow);
+    } else if (cnt <= 1024) {
+        emit_runs<DT, 4>(arr, cnt, p, obase, xrow);
+    } else if (cnt <= 2048) {
+        emit_runs<DT, 8>(arr, cnt, p, obase, xrow);
+    } else {
+        const int P = pow2_ceil(cnt);
+        for (int i = cnt + threadIdx.x; i < P; i += kThreads)
+            arr[i] = 0ull;
+        __syncthreads();
+        bitonic_sort_smem(arr, P, true);
+        for (int i = threadIdx.x; i < cnt; i += kThreads)
+            emit<DT>(p, obase, i, arr[i], xrow);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.
+// ---------------------------------------------------------------------------
+template <int DT, bool BULK, int MAXR>
+__global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Params p)
+{
+    using E = Elem<DT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int S = p.splits;
+    const int row = blockIdx.x / S, slice = blockIdx.x % S;
+
+    unsigned char *ring = smem;
+    unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem + p.off_cand);
+    unsigned long long *perm = reinterpret_cast<unsigned long long *>(smem + p.off_perm);
+    uint32_t *whist = reinterpret_cast<uint32_t *>(smem + p.off_hist);
+    uint16_t *holes = reinterpret_cast<uint16_t *>(smem + p.off_holes);
+    Misc *ms = reinterpret_cast<Misc *>(smem + p.off_misc);
+
+    long long len_ll = p.row_len ? (long long)p.row_len[row] : p.N;
+    len_ll = len_ll < 0 ? 0 : (len_ll > p.N ? p.N : len_ll);
+    const int len = (int)len_ll;
+    const int B = p.B;
+    const int m = (int)((len_ll + B - 1) / B);
+    const int per = (m + S - 1) / S;
+    const int first_block = slice * per;
+    const int msl = max(0, min(per, m - first_block));  // blocks of this slice
+    const unsigned char *xrow =
+        reinterpret_cast<const unsigned char *>(p.x) + (size_t)row * (size_t)p.N * E::kSize;
+
+    // -- random block order: ascending (Philox word 0, block id) -------------
+    const int P = pow2_ceil(msl > 32 ? msl : 32);
+    for (int i = tid; i < P; i += kThreads) {
+        unsigned long long v = ~0ull;
+        if (i < msl) {
+            const uint32_t b = (uint32_t)(first_block + i);
+            const uint32_t w = philox_word0(b, (uint32_t)row, (uint32_t)slice, 0u, p.seed_lo, p.seed_hi);
+            v = ((unsigned long long)w << 32) | b;
+        }
+        perm[i] = v;
+    }
+    for (int i = tid; i < kWarps * 256; i += kThreads)
+        whist[i] = 0u;
+    if (tid == 0) {
+        ms->flag = 0;
+        ms->merge_count = 0;
+        if (BULK) {
+            for (int s = 0; s < p.stages; ++s)
+                mbar_init(smem_addr(&ms->bar[s]), 1u);
+            mbar_fence_init();
+        }
+    }
+    __syncthreads();
+    sort_asc_small(perm, msl, P);
+
+    const int bps = p.bps;
+    const int nst = (msl + bps - 1) / bps;
+    const int esz = E::kSize;
+
+    // warp 0 issues the bulk copies of stage st into ring slot st % stages:
+    // lane g copies block g of the stage, lane 0 first posts the byte count
+    int issued = 0;  // stages issued so far (meaningful in warp 0)
+    auto issue_stage = [&](int st) {
+        issued = st + 1;
+        const int buf = st % p.stages;
+        const uint32_t bar = smem_addr(&ms->bar[buf]);
+        const int q = st * bps + lane;
+        uint32_t nb = 0u;
+        int lo = 0;
+        if (lane < bps && q < msl) {
+            lo = (int)(uint32_t)perm[q] * B;
+            const int hi = min(lo + B, len);
+            nb = (uint32_t)((hi - lo) * esz) & ~15u;
+        }
+        const uint32_t total = __reduce_add_sync(kFull, nb);
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, total);
+        __syncwarp();
+        if (nb)
+            bulk_copy_g2s(smem_addr(ring + (size_t)(buf * bps + lane) * p.slot_bytes),
+                          xrow + (size_t)lo * esz, nb, bar);
+    };
+    if (BULK && warp == 0) {
+        const int pre = min(p.stages, nst);
+        for (int st = 0; st < pre; ++st)
+            issue_stage(st);
+    }
+
+    Threshold thr = threshold_initial<DT>();
+    int n = 0;                              // candidates in the buffer
+    int A = 0, R = 0, W = 0, peak = 0;  // counters of the slice (all below 2^31)
+    bool failed = false;
+    int failed_stage = 0;
+    int ip = 0;                             // parity of the survivor-count buffer
+    const int kB2 = p.k + p.B2;
+    const int g = warp / p.wpb, sub = warp % p.wpb;
+
+    for (int st = 0; st < nst; ++st) {
+        const int buf = BULK ? st % p.stages : 0;
+        if (BULK && !mbar_wait_bounded(smem_addr(&ms->bar[buf]), (uint32_t)((st / p.stages) & 1)))
+            ms->flag = 1;
+
+        BlockView bv;
+        const int q = st * bps + g;
+        const bool has = q < msl;
+        bv.slot = ring + (size_t)(buf * bps + g) * p.slot_bytes;
+        bv.lo = has ? (int)(uint32_t)perm[q] * B : 0;
+        bv.hi = has ? min(bv.lo + B, len) : 0;
+        const int nbytes = (bv.hi - bv.lo) * esz;
+        const int nch = (nbytes + 15) >> 4;
+        bv.c0 = min(sub * p.cpw, nch);
+        bv.c1 = min(bv.c0 + p.cpw, nch);
+
+        // chunks not delivered by a bulk copy (plain-load path, or the ragged
+        // tail of a row) are loaded by the lane that will filter them
+        if (has && (!BULK || (nbytes & 15))) {
+            const int bulk_end = BULK ? (nbytes & ~15) : 0;
+            for (int c = bv.c0 + lane; c < bv.c1; c += 32) {
+                if (c * 16 >= bulk_end) {
+                    unsigned char *dst = const_cast<unsigned char *>(bv.slot) + c * 16;
+                    for (int e = 0; e < E::kPerChunk; ++e) {
+                        const int j = bv.lo + c * E::kPerChunk + e;
+                        if (j < bv.hi) {
+                            if (DT == 0)
+                                reinterpret_cast<uint32_t *>(dst)[e] =
+                                    reinterpret_cast<const uint32_t *>(xrow)[j];
+                            else
+                                reinterpret_cast<uint16_t *>(dst)[e] =
+                                    reinterpret_cast<const uint16_t *>(xrow)[j];
+                        }
+                    }
+                }
+            }
+        }
+
+        int gstart = 0;
+        while (true) {
+            const bool mine = has && g >= gstart;
+            MaskRegs<DT, MAXR> mk;
+            uint32_t lane_cnt = 0u;
+            int cnt = 0;
+            if (mine) {
+                const bool ge = (uint32_t)bv.lo < thr.ti;
+                bv.t = ge ? thr.t_ge : thr.t_gt;
+                bv.refine = ge ? (thr.nan_ge || (uint32_t)bv.hi > thr.ti) : thr.nan_gt;
+                bv.plain = !bv.refine && ((bv.hi - bv.lo) % E::kPerChunk) == 0;
+                cnt = warp_filter<DT, MAXR>(bv, thr, lane, mk, lane_cnt);
+            }
+            int *cw = ms->cntw[ip];
+            ip ^= 1;
+            if (lane == 0)
+                cw[warp] = cnt;
+            const int any = __syncthreads_or(cnt != 0);
+            if (ms->flag) {
+                failed = true;
+                break;
+            }
+            // every thread is past stage st-1: its ring slot can be refilled
+            if (BULK && gstart == 0 && warp == 0 && st > 0 && st - 1 + p.stages < nst) {
+                fence_proxy_async_smem();
+                issue_stage(st - 1 + p.stages);
+            }
+            if (!any)
+                break;
+            // blocks in stage order; find the first one after which the
+            // buffer reaches k + B2
+            int run = n, trig = -1, before_me = 0;
+            {
+                const int4 ca = reinterpret_cast<const int4 *>(cw)[0];
+                const int4 cb = reinterpret_cast<const int4 *>(cw)[1];
+                const int cv[kWarps] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+#pragma unroll
+                for (int w2 = 0; w2 < kWarps; ++w2) {
+                    if (trig < 0 && w2 >= gstart * p.wpb) {
+                        if (w2 < warp)
+                            before_me += cv[w2];
+                        run += cv[w2];
+                        if ((w2 % p.wpb) == p.wpb - 1 && run >= kB2)
+                            trig = w2 / p.wpb;
+                    }
+                }
+            }
+            const int gend = trig >= 0 ? trig : bps - 1;
+            if (mine && g <= gend && cnt)
+                warp_append<DT, MAXR>(bv, lane, mk, lane_cnt, cand, n + before_me);
+            A += run - n;
+            peak = run > peak ? run : peak;
+            n = run;
+            if (trig < 0)
+                break;  // the next barrier orders these appends before any reader
+            W += n;
+            R += 1;
+            __syncthreads();  // every warp's appends are in the buffer
+            const unsigned long long tcomp = radix_select_topk(cand, n, p.k, whist, holes, ms);
+            n = p.k;
+            thr = threshold_from<DT>(tcomp);
+            gstart = trig + 1;
+            if (gstart >= bps)
+                break;
+        }
+        if (failed) {
+            failed_stage = st;
+            break;
+        }
+    }
+
+    if (failed) {
+        // wait (bounded) for every copy still in flight, record the failure
+        // and give up the slice
+        if (tid == 0) {
+            if (BULK)
+                for (int s = failed_stage; s < issued; ++s)
+                    (void)mbar_wait_bounded(smem_addr(&ms->bar[s % p.stages]),
+                                            (uint32_t)((s / p.stages) & 1));
+            atomicOr(p.status, 1u);
+        }
+        n = 0;
+    }
+    __syncthreads();  // appends of the last stage are visible
+
+    // -- final TopK of the slice ---------------------------------------------
+    W += n;
+    if (n > p.k)
+        radix_select_topk(cand, n, p.k, whist, holes, ms);
+    const int cnt = n < p.k ? n : p.k;
+    if (p.stats != nullptr && tid == 0) {
+        long long *s = p.stats + ((long long)row * S + slice) * 4;
+        s[0] = A;
+        s[1] = R;
+        s[2] = W;
+        s[3] = peak;
+    }
+
+    if (S == 1) {
+        sort_and_write<DT>(cand, cnt, p, row, xrow);
+        return;
+    }
+
+    // -- split rows: partial top-k of every slice into CTA 0 -------------------
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
+    if (tid == 0)
+        ms->merge_off = atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), cnt);
+    __syncthreads();
+    unsigned long long *dst =
+        cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
+    for (int i = tid; i < cnt; i += kThreads)
+        dst[i] = cand[i];
+    cluster.sync();
+    if (slice != 0)
+        return;
+    const int total = ms->merge_count;
+    const int kk = total < p.k ? total : p.k;
+    unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
+    if (total > kk)
+        radix_select_topk(merged, total, kk, whist, holes, ms);
+    sort_and_write<DT>(merged, kk, p, row, xrow);
+}
+
+typedef void (*KernelFn)(Params);
+
+// Kernel entry points of one dtype, defined in ds_kernels_<dtype>.cu.
+KernelFn kernel_fp32(bool bulk, bool wide);
+KernelFn kernel_bf16(bool bulk, bool wide);
+
+}  // namespace ds

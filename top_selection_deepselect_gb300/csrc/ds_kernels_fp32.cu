@@ -1,0 +1,13 @@
+// ds_kernels_fp32.cu -- fp32 instantiations of the DeepSelect top-k kernel.
+#include "ds_kernel.cuh"
+
+namespace ds {
+
+KernelFn kernel_fp32(bool bulk, bool wide)
+{
+    if (bulk)
+        return wide ? deepselect_topk_kernel<0, true, 16> : deepselect_topk_kernel<0, true, 4>;
+    return wide ? deepselect_topk_kernel<0, false, 16> : deepselect_topk_kernel<0, false, 4>;
+}
+
+}  // namespace ds

@@ -1,36 +1,10 @@
-// ds_topk.cu -- DeepSelect top-k for GB300 (sm_103a): the streaming kernel
-// and the C-ABI launcher declared in include/ds_topk.h.
-//
-// One CTA (256 threads) scans one row, or one slice of a row when the row is
-// split across the CTAs of a thread-block cluster.  The loop is the one of
-// PFCCLab/DeepSelect "DeepSelect-deep-dive", section "算法":
-//   * the row's B-blocks are visited in a random order drawn from Philox
-//     (independent of the data), each one read from HBM exactly once;
-//   * every element above the running threshold T is appended to a
-//     candidate buffer in shared memory;
-//   * after a block, if the buffer holds k + B2 or more entries, a radix
-//     select shrinks it to k and T becomes the smallest kept element.
-// GB300 mapping:
-//   * blocks are staged into a ring of shared-memory stages by bulk (TMA)
-//     copies issued by one thread, completion tracked by mbarriers, several
-//     stages ahead of the filter;
-//   * a stage holds one B-block per `warps_per_block` warps; each warp filters
-//     its part with one unordered compare per element (fp32 FSETP, bf16 packed
-//     set.geu) and only when a warp sees a survivor does it build exact bit
-//     masks, which are placed with __ffs after a warp prefix sum (section
-//     "实现": one-pass mask + __ffs placement);
-//   * the blocks of a stage are filtered in parallel against the same T; a
-//     stage is cut at the first block after which the buffer would reach
-//     k + B2, the buffer is compacted, and the rest of the stage is filtered
-//     again with the new T -- exactly the block-by-block semantics, so the
-//     counters A, R, W and the peak length equal the step-by-step model's;
-//   * split rows (section "实现", last paragraph): each CTA of the cluster
-//     selects the top k of its contiguous slice and stores it into CTA 0's
-//     shared memory (distributed shared memory), CTA 0 selects and sorts.
+// ds_topk.cu -- host side of the DeepSelect top-k library: argument checks,
+// launch planning (split factor, ring depth, shared-memory layout) and the C
+// ABI declared in include/ds_topk.h.  The kernel itself is in ds_kernel.cuh,
+// instantiated per dtype in ds_kernels_fp32.cu and ds_kernels_bf16.cu.
 
 #include "ds_topk.h"
 
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -38,448 +12,11 @@
 #include <stdio.h>
 #include <string.h>
 
-#include "ds_device.cuh"
-
-namespace cg = cooperative_groups;
+#include "ds_kernel.cuh"
 
 namespace ds {
-
 // Device status word: bit 0 = a kernel gave up waiting for a bulk copy.
 __device__ unsigned int g_status;
-
-struct Params {
-    const void *x;
-    const int32_t *row_len;
-    int32_t *out_idx;
-    void *out_val;
-    long long *stats;
-    long long N;
-    int k, B, B2;
-    uint32_t seed_lo, seed_hi;
-    int splits;          // CTAs per row
-    int wpb;             // warps per B-block
-    int bps;             // B-blocks per stage (kWarps / wpb)
-    int stages;          // ring depth (1 for the plain-load path)
-    int slot_bytes;      // bytes of one staged block (B * size rounded up to 16)
-    int cpw;             // 16-byte chunks per warp of a block
-    int idx_bits;        // index bits that vary (multiple of 8)
-    int off_cand, off_perm, off_hist, off_holes, off_misc;
-};
-
-// ---------------------------------------------------------------------------
-// Filter of one warp's part of a block.
-// ---------------------------------------------------------------------------
-struct BlockView {
-    const unsigned char *slot;  // shared-memory copy of the block
-    int lo, hi;                 // row-local element range [lo, hi)
-    int c0, c1;                 // this warp's 16-byte chunks [c0, c1)
-    uint32_t t;                 // prefilter operand
-    bool refine;                // resolve survivors exactly by composite
-};
-
-template <int DT>
-__device__ __forceinline__ uint32_t prefilter_any(const uint4 v, uint32_t t)
-{
-    if (DT == 0) {
-        const float tf = __uint_as_float(t);
-        const bool p = !(__uint_as_float(v.x) < tf) | !(__uint_as_float(v.y) < tf) |
-                       !(__uint_as_float(v.z) < tf) | !(__uint_as_float(v.w) < tf);
-        return p ? 1u : 0u;
-    } else {
-        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-        return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.x), t2) |
-               __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.y), t2) |
-               __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.z), t2) |
-               __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.w), t2);
-    }
-}
-
-template <int DT>
-__device__ __forceinline__ uint32_t element_bits(const uint4 v, int e)
-{
-    if (DT == 0) {
-        return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
-    } else {
-        const uint32_t w = (e >> 1) == 0 ? v.x : (e >> 1) == 1 ? v.y : (e >> 1) == 2 ? v.z : v.w;
-        return (e & 1) ? (w >> 16) : (w & 0xFFFFu);
-    }
-}
-
-// Exact survivor mask of chunk c (bit e = element lo + c*kPerChunk + e).
-template <int DT>
-__device__ __forceinline__ uint32_t chunk_mask(const uint4 v, int c, const BlockView &bv,
-                                               const Threshold &thr)
-{
-    using E = Elem<DT>;
-    uint32_t mask;
-    if (DT == 0) {
-        const float tf = __uint_as_float(bv.t);
-        mask = (uint32_t)!(__uint_as_float(v.x) < tf) | ((uint32_t)!(__uint_as_float(v.y) < tf) << 1) |
-               ((uint32_t)!(__uint_as_float(v.z) < tf) << 2) |
-               ((uint32_t)!(__uint_as_float(v.w) < tf) << 3);
-    } else {
-        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&bv.t);
-        const uint32_t m0 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.x), t2);
-        const uint32_t m1 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.y), t2);
-        const uint32_t m2 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.z), t2);
-        const uint32_t m3 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.w), t2);
-        mask = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
-               ((m2 & 1u) << 4) | ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
-    }
-    const int first = bv.lo + c * E::kPerChunk;
-    const int valid = bv.hi - first;
-    if (valid < E::kPerChunk)
-        mask &= (1u << valid) - 1u;
-    if (bv.refine && mask) {
-        uint32_t m = mask;
-        while (m) {
-            const int e = __ffs(m) - 1;
-            m &= m - 1u;
-            const unsigned long long comp =
-                ((unsigned long long)E::key(element_bits<DT>(v, e)) << 32) |
-                (unsigned long long)(~(uint32_t)(first + e));
-            if (!(comp > thr.comp))
-                mask &= ~(1u << e);
-        }
-    }
-    return mask;
-}
-
-// Survivors of this warp's chunks (warp total, in every lane).
-template <int DT>
-__device__ __forceinline__ int warp_count(const BlockView &bv, const Threshold &thr, int lane)
-{
-    uint32_t any = 0u;
-    for (int c = bv.c0 + lane; c < bv.c1; c += 32)
-        any |= prefilter_any<DT>(lds128(bv.slot + c * 16), bv.t);
-    if (!__any_sync(kFull, any != 0u))
-        return 0;
-    uint32_t cnt = 0u;
-    for (int c = bv.c0 + lane; c < bv.c1; c += 32)
-        cnt += __popc(chunk_mask<DT>(lds128(bv.slot + c * 16), c, bv, thr));
-    return (int)warp_sum(cnt);
-}
-
-// Appends this warp's survivors at cand[base ...] in chunk order
-// (predicate / exclusive scan / scatter of "Compact", mask walked with __ffs).
-template <int DT>
-__device__ __forceinline__ void warp_append(const BlockView &bv, const Threshold &thr, int lane,
-                                            unsigned long long *cand, int base)
-{
-    using E = Elem<DT>;
-    const int rounds = (bv.c1 - bv.c0 + 31) >> 5;
-    for (int r = 0; r < rounds; ++r) {
-        const int c = bv.c0 + lane + 32 * r;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        uint32_t mask = 0u;
-        if (c < bv.c1) {
-            v = lds128(bv.slot + c * 16);
-            mask = chunk_mask<DT>(v, c, bv, thr);
-        }
-        const uint32_t cnt = __popc(mask);
-        const uint32_t incl = warp_inclusive_scan(cnt, lane);
-        int pos = base + (int)(incl - cnt);
-        const int first = bv.lo + c * E::kPerChunk;
-        while (mask) {
-            const int e = __ffs(mask) - 1;
-            mask &= mask - 1u;
-            cand[pos++] = ((unsigned long long)E::key(element_bits<DT>(v, e)) << 32) |
-                          (unsigned long long)(~(uint32_t)(first + e));
-        }
-        base += (int)__shfl_sync(kFull, incl, 31);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Final order and output: bitonic sort of the cnt selected composites, then
-// index = ~low word and value = the bits the key came from (the input is read
-// again only for +-0 and NaN, whose keys do not determine the bits).
-// ---------------------------------------------------------------------------
-template <int DT>
-__device__ void sort_and_write(unsigned long long *arr, int cnt, const Params &p, int row,
-                               const unsigned char *xrow)
-{
-    using E = Elem<DT>;
-    const int P = pow2_ceil(cnt > 0 ? cnt : 1);
-    for (int i = cnt + threadIdx.x; i < P; i += kThreads)
-        arr[i] = 0ull;
-    __syncthreads();
-    bitonic_sort_u64(arr, P, true);
-    const long long obase = (long long)row * p.k;
-    for (int i = threadIdx.x; i < p.k; i += kThreads) {
-        int32_t idx = -1;
-        uint32_t bits = E::kNegInfBits;
-        if (i < cnt) {
-            const unsigned long long c = arr[i];
-            idx = (int32_t)(~(uint32_t)c);
-            const uint32_t key = (uint32_t)(c >> 32);
-            if (key == E::kNanKey || key == E::kZeroKey)
-                bits = DT == 0 ? reinterpret_cast<const uint32_t *>(xrow)[idx]
-                               : reinterpret_cast<const uint16_t *>(xrow)[idx];
-            else
-                bits = E::bits_of_key(key);
-        }
-        p.out_idx[obase + i] = idx;
-        if (DT == 0)
-            reinterpret_cast<uint32_t *>(p.out_val)[obase + i] = bits;
-        else
-            reinterpret_cast<uint16_t *>(p.out_val)[obase + i] = (uint16_t)bits;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// The kernel.  grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.
-// ---------------------------------------------------------------------------
-template <int DT, bool BULK, bool STATS>
-__global__ void __launch_bounds__(kThreads, 1) deepselect_topk_kernel(const Params p)
-{
-    using E = Elem<DT>;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int S = p.splits;
-    const int row = blockIdx.x / S, slice = blockIdx.x % S;
-
-    unsigned char *ring = smem;
-    unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem + p.off_cand);
-    unsigned long long *perm = reinterpret_cast<unsigned long long *>(smem + p.off_perm);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.off_hist);
-    uint16_t *holes = reinterpret_cast<uint16_t *>(smem + p.off_holes);
-    Misc *ms = reinterpret_cast<Misc *>(smem + p.off_misc);
-
-    long long len_ll = p.row_len ? (long long)p.row_len[row] : p.N;
-    len_ll = len_ll < 0 ? 0 : (len_ll > p.N ? p.N : len_ll);
-    const int len = (int)len_ll;
-    const int B = p.B;
-    const int m = (int)((len_ll + B - 1) / B);
-    const int per = (m + S - 1) / S;
-    const int first_block = slice * per;
-    const int msl = max(0, min(per, m - first_block));  // blocks of this slice
-    const unsigned char *xrow =
-        reinterpret_cast<const unsigned char *>(p.x) + (size_t)row * (size_t)p.N * E::kSize;
-
-    // -- random block order: ascending (Philox word 0, block id) -------------
-    const int P = pow2_ceil(msl > 0 ? msl : 1);
-    for (int i = tid; i < P; i += kThreads) {
-        unsigned long long v = ~0ull;
-        if (i < msl) {
-            const uint32_t b = (uint32_t)(first_block + i);
-            const uint32_t w = philox_word0(b, (uint32_t)row, (uint32_t)slice, 0u, p.seed_lo, p.seed_hi);
-            v = ((unsigned long long)w << 32) | b;
-        }
-        perm[i] = v;
-    }
-    if (tid == 0) {
-        ms->flag = 0;
-        if (BULK) {
-            for (int s = 0; s < p.stages; ++s)
-                mbar_init(smem_addr(&ms->bar[s]), 1u);
-            mbar_fence_init();
-        }
-    }
-    __syncthreads();
-    bitonic_sort_u64(perm, P, false);
-
-    const int bps = p.bps;
-    const int nst = (msl + bps - 1) / bps;
-    const int esz = E::kSize;
-
-    // thread 0 issues the bulk copies of stage st into ring slot st % stages
-    int issued = 0;  // stages issued so far (thread 0)
-    auto issue_stage = [&](int st) {
-        issued = st + 1;
-        const int buf = st % p.stages;
-        const uint32_t bar = smem_addr(&ms->bar[buf]);
-        uint32_t total = 0u;
-        for (int g = 0; g < bps; ++g) {
-            const int q = st * bps + g;
-            if (q < msl) {
-                const int lo = (int)(uint32_t)perm[q] * B;
-                const int hi = min(lo + B, len);
-                total += (uint32_t)((hi - lo) * esz) & ~15u;
-            }
-        }
-        mbar_arrive_expect_tx(bar, total);
-        for (int g = 0; g < bps; ++g) {
-            const int q = st * bps + g;
-            if (q < msl) {
-                const int lo = (int)(uint32_t)perm[q] * B;
-                const int hi = min(lo + B, len);
-                const uint32_t nb = (uint32_t)((hi - lo) * esz) & ~15u;
-                if (nb)
-                    bulk_copy_g2s(smem_addr(ring + (size_t)(buf * bps + g) * p.slot_bytes),
-                                  xrow + (size_t)lo * esz, nb, bar);
-            }
-        }
-    };
-    if (BULK && tid == 0) {
-        const int pre = min(p.stages, nst);
-        for (int st = 0; st < pre; ++st)
-            issue_stage(st);
-    }
-
-    Threshold thr = threshold_initial<DT>();
-    int n = 0;                              // candidates in the buffer
-    long long A = 0, R = 0, W = 0, peak = 0;
-    bool failed = false;
-    int failed_stage = 0;
-    const int kB2 = p.k + p.B2;
-    const int g = warp / p.wpb, sub = warp % p.wpb;
-
-    for (int st = 0; st < nst; ++st) {
-        const int buf = BULK ? st % p.stages : 0;
-        if (BULK && !mbar_wait_bounded(smem_addr(&ms->bar[buf]), (uint32_t)((st / p.stages) & 1)))
-            ms->flag = 1;
-
-        BlockView bv;
-        const int q = st * bps + g;
-        const bool has = q < msl;
-        bv.slot = ring + (size_t)(buf * bps + g) * p.slot_bytes;
-        bv.lo = has ? (int)(uint32_t)perm[q] * B : 0;
-        bv.hi = has ? min(bv.lo + B, len) : 0;
-        const int nbytes = (bv.hi - bv.lo) * esz;
-        const int nch = (nbytes + 15) >> 4;
-        bv.c0 = min(sub * p.cpw, nch);
-        bv.c1 = min(bv.c0 + p.cpw, nch);
-
-        // chunks not delivered by a bulk copy (plain-load path, or the ragged
-        // tail of a row) are loaded by the lane that will filter them
-        if (has) {
-            const int bulk_end = BULK ? (nbytes & ~15) : 0;
-            for (int c = bv.c0 + lane; c < bv.c1; c += 32) {
-                if (c * 16 >= bulk_end) {
-                    unsigned char *dst = const_cast<unsigned char *>(bv.slot) + c * 16;
-                    for (int e = 0; e < E::kPerChunk; ++e) {
-                        const int j = bv.lo + c * E::kPerChunk + e;
-                        if (j < bv.hi) {
-                            if (DT == 0)
-                                reinterpret_cast<uint32_t *>(dst)[e] =
-                                    reinterpret_cast<const uint32_t *>(xrow)[j];
-                            else
-                                reinterpret_cast<uint16_t *>(dst)[e] =
-                                    reinterpret_cast<const uint16_t *>(xrow)[j];
-                        }
-                    }
-                }
-            }
-        }
-
-        int gstart = 0;
-        while (true) {
-            const bool mine = has && g >= gstart;
-            if (mine) {
-                const bool ge = (uint32_t)bv.lo < thr.ti;
-                bv.t = ge ? thr.t_ge : thr.t_gt;
-                bv.refine = ge ? (thr.nan_ge || (uint32_t)bv.hi > thr.ti) : thr.nan_gt;
-            }
-            const int cnt = mine ? warp_count<DT>(bv, thr, lane) : 0;
-            if (lane == 0)
-                ms->cntw[warp] = cnt;
-            const int any = __syncthreads_or(cnt != 0);
-            if (ms->flag) {
-                failed = true;
-                break;
-            }
-            // every thread is past stage st-1: its ring slot can be refilled
-            if (BULK && gstart == 0 && tid == 0 && st > 0 && st - 1 + p.stages < nst) {
-                fence_proxy_async_smem();
-                issue_stage(st - 1 + p.stages);
-            }
-            if (!any)
-                break;
-            // blocks in stage order; find the first one after which the
-            // buffer reaches k + B2
-            int run = n, trig = -1, before_me = 0;
-            for (int w2 = gstart * p.wpb; w2 < bps * p.wpb; ++w2) {
-                const int c = ms->cntw[w2];
-                if (w2 < warp)
-                    before_me += c;
-                run += c;
-                if ((w2 % p.wpb) == p.wpb - 1 && run >= kB2) {
-                    trig = w2 / p.wpb;
-                    break;
-                }
-            }
-            const int gend = trig >= 0 ? trig : bps - 1;
-            if (mine && g <= gend && cnt)
-                warp_append<DT>(bv, thr, lane, cand, n + before_me);
-            A += run - n;
-            peak = run > peak ? run : peak;
-            n = run;
-            __syncthreads();
-            if (trig < 0)
-                break;
-            W += n;
-            R += 1;
-            const unsigned long long tcomp =
-                radix_select_topk<DT>(cand, n, p.k, hist, holes, ms, p.idx_bits);
-            n = p.k;
-            thr = threshold_from<DT>(tcomp);
-            gstart = trig + 1;
-            if (gstart >= bps)
-                break;
-        }
-        if (failed) {
-            failed_stage = st;
-            break;
-        }
-    }
-
-    if (failed) {
-        // wait (bounded) for every copy still in flight, record the failure
-        // and give up the slice
-        if (tid == 0) {
-            if (BULK)
-                for (int s = failed_stage; s < issued; ++s)
-                    (void)mbar_wait_bounded(smem_addr(&ms->bar[s % p.stages]),
-                                            (uint32_t)((s / p.stages) & 1));
-            atomicOr(&g_status, 1u);
-        }
-        n = 0;
-        __syncthreads();
-    }
-
-    // -- final TopK of the slice ---------------------------------------------
-    W += n;
-    if (n > p.k)
-        radix_select_topk<DT>(cand, n, p.k, hist, holes, ms, p.idx_bits);
-    const int cnt = n < p.k ? n : p.k;
-    if (STATS && tid == 0) {
-        long long *s = p.stats + ((long long)row * S + slice) * 4;
-        s[0] = A;
-        s[1] = R;
-        s[2] = W;
-        s[3] = peak;
-    }
-
-    if (S == 1) {
-        sort_and_write<DT>(cand, cnt, p, row, xrow);
-        return;
-    }
-
-    // -- split rows: partial top-k of every slice into CTA 0 -------------------
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
-    unsigned long long *dst =
-        cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) +
-        (size_t)slice * p.k;
-    for (int i = tid; i < p.k; i += kThreads)
-        dst[i] = i < cnt ? cand[i] : 0ull;  // 0 sorts below every real composite
-    if (tid == 0)
-        *cluster.map_shared_rank(&ms->merge_count[slice], 0) = cnt;
-    cluster.sync();
-    if (slice != 0)
-        return;
-    int total = 0;
-    for (int s = 0; s < S; ++s)
-        total += ms->merge_count[s];
-    const int kk = total < p.k ? total : p.k;
-    unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
-    const int nm = S * p.k;
-    if (kk > 0 && nm > kk)
-        radix_select_topk<DT>(merged, nm, kk, hist, holes, ms, p.idx_bits);
-    sort_and_write<DT>(merged, kk, p, row, xrow);
-}
-
 }  // namespace ds
 
 // ===========================================================================
@@ -519,6 +56,7 @@ struct DevInfo {
     int smem_per_sm = 0;   // shared memory per SM
     int smem_reserved = 0; // reserved shared memory per CTA
     unsigned attr_set = 0; // kernels whose smem attribute was raised
+    unsigned int *status = nullptr;  // device address of the status word
 };
 
 constexpr int kMaxDevices = 64;
@@ -549,6 +87,8 @@ int device_info(DevInfo **out, int *dev_out)
         if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
             return fail_cuda(e, "cudaDeviceGetAttribute(reserved smem)");
         d.smem_reserved = v;
+        if ((e = cudaGetSymbolAddress((void **)&d.status, ds::g_status)) != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(status)");
         d.ready = true;
     }
     *out = &d;
@@ -557,25 +97,20 @@ int device_info(DevInfo **out, int *dev_out)
     return DS_OK;
 }
 
-typedef void (*KernelFn)(Params);
+using ds::KernelFn;
 
-KernelFn kernel_for(int dtype, bool bulk, bool stats, int *slot)
+// 8 instantiations: dtype x bulk copies x mask rounds (4 rounds cover blocks
+// of up to 2 KiB per warp, 16 up to 8 KiB per warp).
+KernelFn kernel_for(int dtype, bool bulk, bool wide, int *slot)
 {
-    static const KernelFn table[8] = {
-        ds::deepselect_topk_kernel<0, false, false>, ds::deepselect_topk_kernel<0, false, true>,
-        ds::deepselect_topk_kernel<0, true, false>,  ds::deepselect_topk_kernel<0, true, true>,
-        ds::deepselect_topk_kernel<1, false, false>, ds::deepselect_topk_kernel<1, false, true>,
-        ds::deepselect_topk_kernel<1, true, false>,  ds::deepselect_topk_kernel<1, true, true>,
-    };
-    const int i = dtype * 4 + (bulk ? 2 : 0) + (stats ? 1 : 0);
-    *slot = i;
-    return table[i];
+    *slot = dtype * 4 + (bulk ? 2 : 0) + (wide ? 1 : 0);
+    return dtype == DS_FP32 ? ds::kernel_fp32(bulk, wide) : ds::kernel_bf16(bulk, wide);
 }
 
-int ensure_attributes(DevInfo &d, int dtype, bool bulk, bool stats, KernelFn *fn)
+int ensure_attributes(DevInfo &d, int dtype, bool bulk, bool wide, KernelFn *fn)
 {
     int slot = 0;
-    *fn = kernel_for(dtype, bulk, stats, &slot);
+    *fn = kernel_for(dtype, bulk, wide, &slot);
     std::lock_guard<std::mutex> lock(g_mu);
     if (d.attr_set & (1u << slot))
         return DS_OK;
@@ -618,30 +153,36 @@ struct Plan {
     bool bulk;
 };
 
-int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
 // Shared-memory layout for a given split factor and ring depth.
+// Shared-memory layout for a given split factor and ring depth.  Every region
+// starts on a 128-byte boundary (bulk-copy destinations need 16 bytes, the
+// scratch words are read with 128-bit loads).
+long long align128(long long v) { return (v + 127) / 128 * 128; }
+
 long long layout(Plan &pl, int stages, int splits)
 {
     Params &p = pl.p;
     const long long ring_stream = (long long)stages * p.bps * p.slot_bytes;
     const long long ring_merge = splits > 1 ? (long long)splits * p.k * 8 : 0;
-    long long off = align_up((int)(ring_stream > ring_merge ? ring_stream : ring_merge), 128);
-    const long long cap = (long long)(p.k + (long long)p.B + p.B2) > ds::pow2_ceil(p.k)
-                              ? (long long)p.k + p.B + p.B2
-                              : ds::pow2_ceil(p.k);
+    long long off = align128(ring_stream > ring_merge ? ring_stream : ring_merge);
+    long long cap = (long long)p.k + p.B + p.B2;
+    if (cap < ds::pow2_ceil(p.k))
+        cap = ds::pow2_ceil(p.k);
+    if (cap < 32)
+        cap = 32;
     p.off_cand = (int)off;
-    off += cap * 8;
+    off = align128(off + cap * 8);
     const long long m = (p.N + p.B - 1) / p.B;
     const long long per = (m + splits - 1) / splits;
     p.off_perm = (int)off;
-    off += (long long)ds::pow2_ceil((int)(per > 0 ? per : 1)) * 8;
+    off = align128(off + (long long)ds::pow2_ceil((int)(per > 32 ? per : 32)) * 8);
     p.off_hist = (int)off;
-    off += 2 * 256 * 4;
+    off = align128(off + ds::kWarps * 256 * 4);
     p.off_holes = (int)off;
-    off += align_up(p.k * 2, 16);
+    off = align128(off + (long long)p.k * 2);
     p.off_misc = (int)off;
-    off += align_up((int)sizeof(ds::Misc), 16);
+    off = align128(off + (long long)sizeof(ds::Misc));
     return off;
 }
 
@@ -673,12 +214,6 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     p.wpb = wpb;
     p.bps = ds::kWarps / wpb;
     p.cpw = (p.slot_bytes / 16 + wpb - 1) / wpb;
-    int bits = 1;
-    while (bits < 31 && ((long long)1 << bits) < N)
-        ++bits;
-    p.idx_bits = (bits + 7) / 8 * 8;
-    if (p.idx_bits > 32)
-        p.idx_bits = 32;
 
     const long long m = (N + B - 1) / B;
     const long long budget_one = d.smem_optin;
@@ -813,7 +348,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     if ((rc = make_plan(x, dtype, rows, N, k, B, B2, splits_req, stats != nullptr, *d, pl)) != DS_OK)
         return rc;
     KernelFn fn = nullptr;
-    if ((rc = ensure_attributes(*d, dtype, pl.bulk, stats != nullptr, &fn)) != DS_OK)
+    if ((rc = ensure_attributes(*d, dtype, pl.bulk, pl.p.cpw > 128, &fn)) != DS_OK)
         return rc;
     // a cluster must fit on one GPC: shrink an automatic split factor until
     // the hardware can hold at least one cluster
@@ -840,6 +375,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     p.out_idx = out_idx;
     p.out_val = out_val;
     p.stats = reinterpret_cast<long long *>(stats);
+    p.status = d->status;
     p.seed_lo = (uint32_t)seed;
     p.seed_hi = (uint32_t)(seed >> 32);
 
