@@ -19,14 +19,13 @@
  *
  * Memory: every pointer passed to ds_topk / ds_topk_ex is device memory owned
  * by the caller.  The library allocates nothing on the device and keeps no
- * per-call state; it caches a few attributes per device and reports device
- * time-outs through a per-device status word (ds_topk_device_status).
+ * per-call state; it caches a few attributes per device.
  *
  * Layout: x is row-major with a row pitch of N elements; row r starts at
  * element r*N.  Outputs are row-major [rows][k].  Any alignment of x works;
  * when x is 16-byte aligned and N*sizeof(elem) and B*sizeof(elem) are
- * multiples of 16 the rows are staged into shared memory by bulk (TMA)
- * copies, otherwise by plain loads.
+ * multiples of 16 the rows are staged into shared memory by 16-byte
+ * asynchronous copies several stages ahead, otherwise by plain loads.
  *
  * Asynchrony: ds_topk and ds_topk_ex only enqueue work on `stream` (a
  * cudaStream_t, NULL for the legacy default stream) and return; they never
@@ -51,7 +50,6 @@ extern "C" {
 #define DS_EINVAL (-1)       /* an argument is out of range or a pointer is NULL */
 #define DS_EUNSUPPORTED (-2) /* dtype unknown, or the working set does not fit in shared memory */
 #define DS_ECUDA (-3)        /* a CUDA runtime call failed (see ds_last_error_detail) */
-#define DS_EDEVICE (-4)      /* a kernel gave up waiting for a copy (device status word set) */
 
 #define DS_FP32 0
 #define DS_BF16 1
@@ -60,10 +58,10 @@ extern "C" {
 typedef struct {
     int splits;           /* CTAs cooperating on one row (thread-block cluster size) */
     int threads;          /* threads per CTA */
-    int stages;           /* shared-memory ring depth, in stages */
+    int stages;           /* shared-memory ring slots, in stages */
     int blocks_per_stage; /* B-blocks staged per ring stage */
     int warps_per_block;  /* warps filtering one B-block */
-    int bulk;             /* 1: bulk (TMA) copies into shared memory; 0: plain loads */
+    int async_copy;       /* 1: 16-byte asynchronous copies into shared memory; 0: plain loads */
     int smem_bytes;       /* dynamic shared memory per CTA */
     int capacity;         /* candidate-buffer capacity in entries (>= k + B + B2) */
     int grid;             /* CTAs launched (rows * splits) */
@@ -131,11 +129,6 @@ int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, in
  * the current device (N taken as large as the block order allows), or a
  * negative status. */
 int ds_topk_max_k(int dtype, int B, int B2);
-
-/* Reads and clears the current device's status word: DS_OK, or DS_EDEVICE if
- * a kernel gave up waiting for a bulk copy since the last read.
- * Synchronises the device. */
-int ds_topk_device_status(void);
 
 /* Fixed description of a status code. */
 const char *ds_strerror(int status);

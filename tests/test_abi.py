@@ -43,7 +43,7 @@ def test_library_is_built_for_sm_103a(lib):
 
 
 def test_strerror_texts(lib):
-    for status in [ds.DS_OK, ds.DS_EINVAL, ds.DS_EUNSUPPORTED, ds.DS_ECUDA, ds.DS_EDEVICE]:
+    for status in [ds.DS_OK, ds.DS_EINVAL, ds.DS_EUNSUPPORTED, ds.DS_ECUDA]:
         assert ds.ds_strerror(status)
     assert ds.ds_strerror(-99) == "unknown status"
 

@@ -30,7 +30,6 @@ def library():
     _ds.load_library()
     ds = _ds
     yield
-    assert ds.ds_topk_device_status() == ds.DS_OK
 
 
 DEV = "cuda:0"
@@ -203,7 +202,7 @@ def test_misaligned_input_pointer(dtype):
     out_val = torch.empty((rows, k), dtype=xt.dtype, device=DEV)
     code = ds.DS_FP32 if dtype == "fp32" else ds.DS_BF16
     plan = ds.ds_topk_plan(xt.data_ptr() + esz, code, rows, N, k, 256, 256, 1)
-    assert plan["bulk"] == 0
+    assert plan["async_copy"] == 0
     ds.ds_topk_ex(xt.data_ptr() + esz, code, rows, None, N, k, 256, 256, 7, 1,
                   out_idx.data_ptr(), out_val.data_ptr(), None, None)
     torch.cuda.synchronize()
@@ -276,6 +275,6 @@ def test_plans_of_the_workloads():
         c = workloads.CONFIGS[name]
         code = ds.DS_FP32 if c["dtype"] == "fp32" else ds.DS_BF16
         plan = ds.ds_topk_plan(1 << 20, code, c["rows"], c["N"], c["k"], c["B"], c["B2"], 0)
-        assert plan["bulk"] == 1
+        assert plan["async_copy"] == 1
         assert plan["capacity"] >= c["k"] + c["B"] + c["B2"]
         assert plan["grid"] == c["rows"] * plan["splits"]

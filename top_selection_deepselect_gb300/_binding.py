@@ -17,12 +17,11 @@ DS_OK = 0
 DS_EINVAL = -1
 DS_EUNSUPPORTED = -2
 DS_ECUDA = -3
-DS_EDEVICE = -4
 DS_FP32 = 0
 DS_BF16 = 1
 
 ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_plan", "ds_topk_max_k",
-                "ds_topk_device_status", "ds_strerror", "ds_last_error_detail"]
+                "ds_strerror", "ds_last_error_detail"]
 
 
 class DSError(RuntimeError):
@@ -36,7 +35,7 @@ class DSError(RuntimeError):
 
 class ds_plan_t(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in
-                ("splits", "threads", "stages", "blocks_per_stage", "warps_per_block", "bulk",
+                ("splits", "threads", "stages", "blocks_per_stage", "warps_per_block", "async_copy",
                  "smem_bytes", "capacity", "grid", "ctas_per_sm")]
 
     def as_dict(self):
@@ -74,8 +73,6 @@ def load_library(path=None):
         lib.ds_topk_plan.restype = i32
         lib.ds_topk_max_k.argtypes = [i32, i32, i32]
         lib.ds_topk_max_k.restype = i32
-        lib.ds_topk_device_status.argtypes = []
-        lib.ds_topk_device_status.restype = i32
         lib.ds_strerror.argtypes = [i32]
         lib.ds_strerror.restype = ctypes.c_char_p
         lib.ds_last_error_detail.argtypes = []
@@ -136,10 +133,6 @@ def ds_topk_max_k(dtype, B, B2):
     if r < 0:
         _check(r, "ds_topk_max_k")
     return r
-
-
-def ds_topk_device_status():
-    return load_library().ds_topk_device_status()
 
 
 def ds_strerror(status):

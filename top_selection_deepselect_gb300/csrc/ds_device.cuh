@@ -1,6 +1,6 @@
 // ds_device.cuh -- device-side building blocks of the DeepSelect top-k kernel
-// for sm_103a: order keys, Philox4x32-10, mbarrier / bulk-copy wrappers, warp
-// scans, the shared-memory radix select and the bitonic sort.
+// for sm_103a: order keys, Philox4x32-10, asynchronous-copy wrappers, warp
+// scans, the shared-memory radix select and the ordering of the final k.
 //
 // Sources (page title, section):
 //   PFCCLab/DeepSelect "DeepSelect-deep-dive", "算法" (scan / filter /
@@ -25,7 +25,6 @@ constexpr int kWarps = kThreads / 32;     // warps per CTA
 constexpr int kMaxStages = 4;             // deepest shared-memory ring
 constexpr int kMaxSplits = 16;            // largest thread-block cluster used
 constexpr unsigned kFull = 0xFFFFFFFFu;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // bound on any mbarrier wait
 
 // ---------------------------------------------------------------------------
 // Element traits.  A candidate is one 64-bit composite
@@ -167,77 +166,35 @@ __device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint3
 }
 
 // ---------------------------------------------------------------------------
-// PTX wrappers: shared-memory address, global timer, mbarrier, bulk copy.
+// PTX wrappers: shared-memory address, asynchronous copies, 128-bit loads.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ unsigned long long global_timer_ns()
+// 16-byte asynchronous copy global -> shared (L1 bypassed); both addresses
+// 16-byte aligned.  Completion is tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+__device__ __forceinline__ void cp_async_commit()
 {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_fence_init()
+// Waits until at most `pending` (0..3) of this thread's newest commit groups
+// are still in flight.
+__device__ __forceinline__ void cp_async_wait_pending(int pending)
 {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return done != 0u;
-}
-
-// Waits for phase `parity` of the barrier; gives up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity)
-{
-    if (mbar_try_wait(bar, parity))
-        return true;
-    const unsigned long long t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs)
-            return false;
+    switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
     }
-    return true;
-}
-
-// Bulk (TMA, non-tensor) copy global -> own shared memory, completion
-// counted in bytes on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Orders earlier generic-proxy shared-memory accesses before later bulk copies.
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ uint4 lds128(const unsigned char *p)
@@ -467,7 +424,6 @@ __device__ __forceinline__ void sort_asc_small(unsigned long long *a, int cnt, i
 
 // Shared scratch words of one CTA.
 struct Misc {
-    unsigned long long bar[kMaxStages];  // one mbarrier per ring stage
     unsigned long long wor[kWarps];      // per-warp OR / AND / min of composites
     unsigned long long wand[kWarps];
     unsigned long long wmin[kWarps];
@@ -477,10 +433,17 @@ struct Misc {
     uint32_t wsum[kWarps];               // per-warp totals of block scans
     uint32_t sel_digit, sel_above, sel_eq;
     int group_count;
-    int flag;                            // a wait timed out
     int merge_count;                     // CTA 0 of a cluster: entries received
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
+    int fill;                            // select: slots handed out in the compaction
+    int pass;                            // select: digit passes so far (histogram rotation)
+    unsigned long long tmin;             // select: smallest selected composite
 };
+
+// Per-warp 256-bin histograms of 16-bit counters, three rotating buffers.
+constexpr int kHistWordsPerWarp = 128;                     // 256 x u16
+constexpr int kHistBufWords = kWarps * kHistWordsPerWarp;  // one buffer
+constexpr int kHistWords = 3 * kHistBufWords;              // 12 KiB
 
 // Exclusive scan of one value per thread over the CTA (thread order).
 // Uses ms->wsum; ends synchronised.  Returns the exclusive prefix.
@@ -521,9 +484,88 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, Misc *ms)
 //     selected entry its slot in cand[0, k); all entries are in registers, so
 //     the buffer is overwritten in place.
 // ---------------------------------------------------------------------------
+// One digit pass's decision, computed by every warp from the eight per-warp
+// histograms of buffer `hb` (16-bit counters, two per word): lane l owns
+// bins 8l .. 8l+7, lanes are scanned from the top bin down.  Returns the
+// digit holding the need-th entry, the count above it and its own count.
+__device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, int lane,
+                                             uint32_t &dsel, uint32_t &above, uint32_t &eq)
+{
+    uint32_t acc[4] = {0u, 0u, 0u, 0u};  // packed pairs of bin counts (no carry: n < 65536)
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(hb + w * kHistWordsPerWarp + lane * 4);
+        acc[0] += q.x;
+        acc[1] += q.y;
+        acc[2] += q.z;
+        acc[3] += q.w;
+    }
+    uint32_t c[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        c[2 * i] = acc[i] & 0xFFFFu;
+        c[2 * i + 1] = acc[i] >> 16;
+    }
+    uint32_t s = 0;
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+        s += c[t];
+    // suffix sum over lanes (lanes above hold higher bins)
+    uint32_t suf = s;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_down_sync(kFull, suf, d);
+        if (lane + d < 32)
+            suf += o;
+    }
+    const uint32_t excl = suf - s;
+    uint32_t my_d = 0, my_above = 0, my_eq = 0;
+    const bool found = excl < need && need <= suf;
+    if (found) {
+        uint32_t cum = excl;
+#pragma unroll
+        for (int t = 7; t >= 0; --t) {
+            if (my_eq == 0u && cum + c[t] >= need) {
+                my_d = (uint32_t)(8 * lane + t);
+                my_above = cum;
+                my_eq = c[t];
+            }
+            cum += c[t];
+        }
+    }
+    const int src = __ffs(__ballot_sync(kFull, found)) - 1;
+    dsel = __shfl_sync(kFull, my_d, src);
+    above = __shfl_sync(kFull, my_above, src);
+    eq = __shfl_sync(kFull, my_eq, src);
+}
+
+// ---------------------------------------------------------------------------
+// RadixSelectTopK ("算法", step 3) on n > k distinct composites in shared
+// memory.  After the call cand[0, k) holds the k largest (in no particular
+// order); returns the smallest of them, the new threshold.  Called by all
+// threads; ends synchronised.
+//
+// Every thread loads its entries cand[tid + 256j] into registers once (up to
+// R of them); all passes then work on registers:
+//  1. OR and AND of all composites: only bits where they differ can separate
+//     entries, so digits start at the highest such bit and skip bits that
+//     never vary.
+//  2. Digit passes of 8 bits from the top: each warp counts the entries that
+//     still match the chosen prefix into its own 256-bin histogram (shared
+//     atomics on 16-bit counters); after one barrier every warp sums the
+//     eight histograms and finds the digit holding the k-th entry by itself,
+//     so a pass costs a single barrier.  Buffers rotate over three so that a
+//     warp can clear the next one while others still read the last.
+//  3. The loop stops when every entry matching the prefix is needed, or when
+//     at most 32 remain tied; these are gathered and every warp ranks them
+//     to find the exact k-th composite.
+//  4. Compaction: each warp takes a run of slots in cand[0, k) with one
+//     shared atomic and its lanes fill it (positions from a warp scan); all
+//     entries are in registers, so the buffer is overwritten in place.
+// ---------------------------------------------------------------------------
 template <int R>
 static __device__ __noinline__ unsigned long long radix_select_regs(unsigned long long *cand, int n,
-                                                                    int k, uint32_t *whist,
+                                                                    int k, uint32_t *hist,
                                                                     Misc *ms)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -538,6 +580,7 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
             valid |= 1u << j;
         }
     }
+    int pass = ms->pass;  // published before the previous barrier
 
     // 1. varying bits
     unsigned long long vo = 0ull, va = ~0ull;
@@ -554,9 +597,12 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         ms->wor[warp] = vo;
         ms->wand[warp] = va;
     }
-    if (tid == 0)
+    __syncthreads();  // also: all loads of cand are done, every warp read ms->pass
+    if (tid == 0) {
         ms->group_count = 0;
-    __syncthreads();
+        ms->fill = 0;
+        ms->tmin = ~0ull;
+    }
     vo = 0ull;
     va = ~0ull;
 #pragma unroll
@@ -572,32 +618,26 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
     uint32_t need = (uint32_t)k;
     uint32_t live = valid;  // entries still matching the prefix
     int h = 63 - __clzll((long long)vary);
-    uint32_t *wh = whist + warp * 256;
     while (true) {
         const int lo = h >= 7 ? h - 7 : 0;
+        uint32_t *cur = hist + (pass % 3) * kHistBufWords;
+        uint32_t *nxt = hist + ((pass + 1) % 3) * kHistBufWords;
+        uint32_t *mine = cur + warp * kHistWordsPerWarp;
 #pragma unroll
-        for (int j = 0; j < R; ++j)
-            if (live & (1u << j))
-                atomicAdd(&wh[(uint32_t)(v[j] >> lo) & 255u], 1u);
-        __syncthreads();
-        // thread t owns bin 255 - t: scanning in thread order walks the bins
-        // from the top down
-        const int bin = 255 - tid;
-        uint32_t cnt = 0;
+        for (int i = 0; i < kHistWordsPerWarp / 32; ++i)
+            nxt[warp * kHistWordsPerWarp + i * 32 + lane] = 0u;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            cnt += whist[w * 256 + bin];
-            whist[w * 256 + bin] = 0u;
-        }
-        const uint32_t excl = block_exclusive_scan(cnt, ms);
-        if (excl < need && need <= excl + cnt) {
-            ms->sel_digit = (uint32_t)bin;
-            ms->sel_above = excl;
-            ms->sel_eq = cnt;
+        for (int j = 0; j < R; ++j) {
+            if (live & (1u << j)) {
+                const uint32_t d = (uint32_t)(v[j] >> lo) & 255u;
+                atomicAdd(&mine[d >> 1], 1u << ((d & 1u) << 4));
+            }
         }
         __syncthreads();
-        const uint32_t dsel = ms->sel_digit, eq = ms->sel_eq;
-        need -= ms->sel_above;
+        uint32_t dsel, above, eq;
+        digit_search(cur, need, lane, dsel, above, eq);
+        ++pass;
+        need -= above;
         prefix |= (unsigned long long)dsel << lo;
         pmask |= 255ull << lo;
 #pragma unroll
@@ -607,32 +647,25 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         if (eq == need)
             break;
         if (eq <= 32u) {
-            // rank the tied entries directly
-            uint32_t mine = (uint32_t)__popc(live);
-            const uint32_t wcount = __reduce_add_sync(kFull, mine);
-            int wbase = 0;
-            if (lane == 0 && wcount)
-                wbase = atomicAdd(&ms->group_count, (int)wcount);
-            wbase = __shfl_sync(kFull, wbase, 0);
-            int off = wbase + (int)(warp_inclusive_scan(mine, lane) - mine);
+            // gather the tied entries, then every warp ranks them
+            const uint32_t cnt = (uint32_t)__popc(live);
+            const uint32_t incl = warp_inclusive_scan(cnt, lane);
+            int base = 0;
+            if (lane == 31 && incl)
+                base = atomicAdd(&ms->group_count, (int)incl);
+            base = __shfl_sync(kFull, base, 31);
+            int off = base + (int)(incl - cnt);
 #pragma unroll
             for (int j = 0; j < R; ++j)
                 if (live & (1u << j))
                     ms->group[off++] = v[j];
             __syncthreads();
-            if (warp == 0) {
-                const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
-                uint32_t rank = 0;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const unsigned long long o = shfl_xor_u64(g, j) ;
-                    rank += (((lane ^ j) < (int)eq) && o > g) ? 1u : 0u;
-                }
-                if (lane < (int)eq && rank == need - 1u)
-                    ms->texact = g;
-            }
-            __syncthreads();
-            texact = ms->texact;
+            const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
+            uint32_t rank = 0;
+            for (uint32_t j = 0; j < eq; ++j)
+                rank += ms->group[j] > g ? 1u : 0u;
+            const uint32_t bal = __ballot_sync(kFull, lane < (int)eq && rank == need - 1u);
+            texact = __shfl_sync(kFull, g, __ffs(bal) - 1);
             exact = true;
             break;
         }
@@ -656,22 +689,26 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
             }
         }
     }
-    mn = warp_min_reduce(mn);
-    if (lane == 0)
-        ms->wmin[warp] = mn;
-    uint32_t pos = block_exclusive_scan((uint32_t)__popc(sel), ms);  // all loads are done
+    const uint32_t cnt = (uint32_t)__popc(sel);
+    const uint32_t incl = warp_inclusive_scan(cnt, lane);
+    int base = 0;
+    if (lane == 31 && incl)
+        base = atomicAdd(&ms->fill, (int)incl);
+    base = __shfl_sync(kFull, base, 31);
+    int pos = base + (int)(incl - cnt);
 #pragma unroll
     for (int j = 0; j < R; ++j)
         if (sel & (1u << j))
             cand[pos++] = v[j];
+    if (!exact) {
+        mn = warp_min_reduce(mn);
+        if (lane == 0 && mn != ~0ull)
+            atomicMin(&ms->tmin, mn);
+    }
+    if (tid == 0)
+        ms->pass = pass;
     __syncthreads();
-    if (exact)
-        return texact;
-    unsigned long long t = ~0ull;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-        t = min_u64(t, ms->wmin[w]);
-    return t;
+    return exact ? texact : ms->tmin;
 }
 
 // The same for sets too large for registers: every pass reads shared memory.
@@ -680,6 +717,10 @@ static __device__ __noinline__ unsigned long long radix_select_smem(unsigned lon
                                                                     uint16_t *holes, Misc *ms)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // this variant counts in 32-bit words over the histogram region; start
+    // from zero (it leaves the region zero for the rotating buffers)
+    for (int i = tid; i < kHistWords; i += kThreads)
+        whist[i] = 0u;
     unsigned long long vo = 0ull, va = ~0ull;
     for (int i = tid; i < n; i += kThreads) {
         const unsigned long long c = cand[i];
@@ -777,16 +818,16 @@ static __device__ __noinline__ unsigned long long radix_select_smem(unsigned lon
 }
 
 __device__ __forceinline__ unsigned long long radix_select_topk(unsigned long long *cand, int n, int k,
-                                                                uint32_t *whist, uint16_t *holes,
+                                                                uint32_t *hist, uint16_t *holes,
                                                                 Misc *ms)
 {
     if (n <= 8 * kThreads)
-        return radix_select_regs<8>(cand, n, k, whist, ms);
+        return radix_select_regs<8>(cand, n, k, hist, ms);
     if (n <= 12 * kThreads)
-        return radix_select_regs<12>(cand, n, k, whist, ms);
+        return radix_select_regs<12>(cand, n, k, hist, ms);
     if (n <= 24 * kThreads)
-        return radix_select_regs<24>(cand, n, k, whist, ms);
-    return radix_select_smem(cand, n, k, whist, holes, ms);
+        return radix_select_regs<24>(cand, n, k, hist, ms);
+    return radix_select_smem(cand, n, k, hist, holes, ms);
 }
 
 }  // namespace ds

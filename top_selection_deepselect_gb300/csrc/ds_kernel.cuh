@@ -10,9 +10,10 @@
 //   * after a block, if the buffer holds k + B2 or more entries, a radix
 //     select shrinks it to k and T becomes the smallest kept element.
 // GB300 mapping:
-//   * blocks are staged into a ring of shared-memory stages by bulk (TMA)
-//     copies issued by the lanes of one warp, completion tracked by mbarriers, several
-//     stages ahead of the filter;
+//   * blocks are staged into a ring of shared-memory stages several stages
+//     ahead of the filter by 16-byte asynchronous copies (cp.async): each
+//     lane copies exactly the chunks it will filter and waits only on its
+//     own copy groups, so the ring needs no barrier of its own;
 //   * a stage holds one B-block per `warps_per_block` warps; each warp filters
 //     its part with one unordered compare per element (fp32 FSETP, bf16 packed
 //     set.geu); only chunks that may hold a survivor get exact bit masks,
@@ -44,14 +45,14 @@ struct Params {
     int32_t *out_idx;
     void *out_val;
     long long *stats;     // counters {A, R, W, peak} per (row, slice), or null
-    unsigned int *status; // device status word: bit 0 = a wait timed out
     long long N;
     int k, B, B2;
     uint32_t seed_lo, seed_hi;
     int splits;          // CTAs per row
-    int wpb;             // warps per B-block
+    int wpb;             // warps per B-block (a power of two)
+    int wpb_shift;       // log2(wpb)
     int bps;             // B-blocks per stage (kWarps / wpb)
-    int stages;          // ring depth (1 for the plain-load path)
+    int stages;          // ring slots (1 for the plain-load path)
     int slot_bytes;      // bytes of one staged block (B * size rounded up to 16)
     int cpw;             // 16-byte chunks per warp of a block
     int off_cand, off_perm, off_hist, off_holes, off_misc;
@@ -337,7 +338,7 @@ __device__ void sort_and_write(unsigned long long *arr, int cnt, const Params &p
 // ---------------------------------------------------------------------------
 // The kernel.  grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.
 // ---------------------------------------------------------------------------
-template <int DT, bool BULK, int MAXR>
+template <int DT, bool ASYNC, int MAXR>
 __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Params p)
 {
     using E = Elem<DT>;
@@ -375,16 +376,11 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
         }
         perm[i] = v;
     }
-    for (int i = tid; i < kWarps * 256; i += kThreads)
+    for (int i = tid; i < kHistWords; i += kThreads)
         whist[i] = 0u;
     if (tid == 0) {
-        ms->flag = 0;
         ms->merge_count = 0;
-        if (BULK) {
-            for (int s = 0; s < p.stages; ++s)
-                mbar_init(smem_addr(&ms->bar[s]), 1u);
-            mbar_fence_init();
-        }
+        ms->pass = 0;
     }
     __syncthreads();
     sort_asc_small(perm, msl, P);
@@ -392,67 +388,65 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
     const int bps = p.bps;
     const int nst = (msl + bps - 1) / bps;
     const int esz = E::kSize;
+    const int g = warp >> p.wpb_shift, sub = warp & (p.wpb - 1);
+    const int NS = ASYNC ? p.stages : 1;  // ring slots
 
-    // warp 0 issues the bulk copies of stage st into ring slot st % stages:
-    // lane g copies block g of the stage, lane 0 first posts the byte count
-    int issued = 0;  // stages issued so far (meaningful in warp 0)
-    auto issue_stage = [&](int st) {
-        issued = st + 1;
-        const int buf = st % p.stages;
-        const uint32_t bar = smem_addr(&ms->bar[buf]);
-        const int q = st * bps + lane;
-        uint32_t nb = 0u;
-        int lo = 0;
-        if (lane < bps && q < msl) {
-            lo = (int)(uint32_t)perm[q] * B;
-            const int hi = min(lo + B, len);
-            nb = (uint32_t)((hi - lo) * esz) & ~15u;
+    // Every lane copies its own 16-byte chunks of this warp's part of the
+    // block at stage st into ring slot `slot` with cp.async and commits one
+    // group per stage (possibly empty).  A lane later reads only chunks it
+    // copied itself, so waiting on its own groups is all the synchronisation
+    // the ring needs.  The partial last chunk of a row is loaded at use.
+    auto prefetch = [&](int st, int slot) {
+        const int q = st * bps + g;
+        if (st < nst && q < msl) {
+            const int lo = (int)(uint32_t)perm[q] * B;
+            const int nbytes = (min(lo + B, len) - lo) * esz;
+            const int nch = (nbytes + 15) >> 4;
+            const int c0 = min(sub * p.cpw, nch), c1 = min(c0 + p.cpw, nch);
+            unsigned char *dst = ring + (size_t)(slot * bps + g) * p.slot_bytes;
+            const unsigned char *src = xrow + (size_t)lo * esz;
+            for (int c = c0 + lane; c < c1; c += 32)
+                if ((c + 1) * 16 <= nbytes)
+                    cp_async16(smem_addr(dst + c * 16), src + c * 16);
         }
-        const uint32_t total = __reduce_add_sync(kFull, nb);
-        if (lane == 0)
-            mbar_arrive_expect_tx(bar, total);
-        __syncwarp();
-        if (nb)
-            bulk_copy_g2s(smem_addr(ring + (size_t)(buf * bps + lane) * p.slot_bytes),
-                          xrow + (size_t)lo * esz, nb, bar);
+        cp_async_commit();
     };
-    if (BULK && warp == 0) {
-        const int pre = min(p.stages, nst);
-        for (int st = 0; st < pre; ++st)
-            issue_stage(st);
-    }
+    if (ASYNC)
+        for (int s = 0; s < NS - 1; ++s)
+            prefetch(s, s);
 
     Threshold thr = threshold_initial<DT>();
-    int n = 0;                              // candidates in the buffer
+    int n = 0;                          // candidates in the buffer
     int A = 0, R = 0, W = 0, peak = 0;  // counters of the slice (all below 2^31)
-    bool failed = false;
-    int failed_stage = 0;
-    int ip = 0;                             // parity of the survivor-count buffer
+    int ip = 0;                         // parity of the survivor-count buffer
+    int slot = 0;                       // ring slot of the current stage
     const int kB2 = p.k + p.B2;
-    const int g = warp / p.wpb, sub = warp % p.wpb;
 
     for (int st = 0; st < nst; ++st) {
-        const int buf = BULK ? st % p.stages : 0;
-        if (BULK && !mbar_wait_bounded(smem_addr(&ms->bar[buf]), (uint32_t)((st / p.stages) & 1)))
-            ms->flag = 1;
+        if (ASYNC) {
+            // refill the slot this lane finished with (stage st-1)
+            prefetch(st + NS - 1, slot == 0 ? NS - 1 : slot - 1);
+            cp_async_wait_pending(NS - 1);  // this lane's copies of stage st landed
+        }
 
         BlockView bv;
         const int q = st * bps + g;
         const bool has = q < msl;
-        bv.slot = ring + (size_t)(buf * bps + g) * p.slot_bytes;
+        bv.slot = ring + (size_t)(slot * bps + g) * p.slot_bytes;
         bv.lo = has ? (int)(uint32_t)perm[q] * B : 0;
         bv.hi = has ? min(bv.lo + B, len) : 0;
         const int nbytes = (bv.hi - bv.lo) * esz;
         const int nch = (nbytes + 15) >> 4;
         bv.c0 = min(sub * p.cpw, nch);
         bv.c1 = min(bv.c0 + p.cpw, nch);
+        slot = slot + 1 == NS ? 0 : slot + 1;
 
-        // chunks not delivered by a bulk copy (plain-load path, or the ragged
-        // tail of a row) are loaded by the lane that will filter them
-        if (has && (!BULK || (nbytes & 15))) {
-            const int bulk_end = BULK ? (nbytes & ~15) : 0;
+        // chunks not copied ahead (plain-load path, or the ragged tail of a
+        // row) are loaded by the lane that will filter them
+        if (has && (!ASYNC || (nbytes & 15))) {
+            const int async_end = ASYNC ? (nbytes & ~15) : 0;
             for (int c = bv.c0 + lane; c < bv.c1; c += 32) {
-                if (c * 16 >= bulk_end) {
+                if (c * 16 >= async_end) {
                     unsigned char *dst = const_cast<unsigned char *>(bv.slot) + c * 16;
                     for (int e = 0; e < E::kPerChunk; ++e) {
                         const int j = bv.lo + c * E::kPerChunk + e;
@@ -479,24 +473,14 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
                 const bool ge = (uint32_t)bv.lo < thr.ti;
                 bv.t = ge ? thr.t_ge : thr.t_gt;
                 bv.refine = ge ? (thr.nan_ge || (uint32_t)bv.hi > thr.ti) : thr.nan_gt;
-                bv.plain = !bv.refine && ((bv.hi - bv.lo) % E::kPerChunk) == 0;
+                bv.plain = !bv.refine && ((bv.hi - bv.lo) & (E::kPerChunk - 1)) == 0;
                 cnt = warp_filter<DT, MAXR>(bv, thr, lane, mk, lane_cnt);
             }
             int *cw = ms->cntw[ip];
             ip ^= 1;
             if (lane == 0)
                 cw[warp] = cnt;
-            const int any = __syncthreads_or(cnt != 0);
-            if (ms->flag) {
-                failed = true;
-                break;
-            }
-            // every thread is past stage st-1: its ring slot can be refilled
-            if (BULK && gstart == 0 && warp == 0 && st > 0 && st - 1 + p.stages < nst) {
-                fence_proxy_async_smem();
-                issue_stage(st - 1 + p.stages);
-            }
-            if (!any)
+            if (!__syncthreads_or(cnt != 0))
                 break;
             // blocks in stage order; find the first one after which the
             // buffer reaches k + B2
@@ -505,14 +489,15 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
                 const int4 ca = reinterpret_cast<const int4 *>(cw)[0];
                 const int4 cb = reinterpret_cast<const int4 *>(cw)[1];
                 const int cv[kWarps] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+                const int wmask = p.wpb - 1;
 #pragma unroll
                 for (int w2 = 0; w2 < kWarps; ++w2) {
-                    if (trig < 0 && w2 >= gstart * p.wpb) {
+                    if (trig < 0 && w2 >= (gstart << p.wpb_shift)) {
                         if (w2 < warp)
                             before_me += cv[w2];
                         run += cv[w2];
-                        if ((w2 % p.wpb) == p.wpb - 1 && run >= kB2)
-                            trig = w2 / p.wpb;
+                        if ((w2 & wmask) == wmask && run >= kB2)
+                            trig = w2 >> p.wpb_shift;
                     }
                 }
             }
@@ -534,24 +519,9 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
             if (gstart >= bps)
                 break;
         }
-        if (failed) {
-            failed_stage = st;
-            break;
-        }
     }
-
-    if (failed) {
-        // wait (bounded) for every copy still in flight, record the failure
-        // and give up the slice
-        if (tid == 0) {
-            if (BULK)
-                for (int s = failed_stage; s < issued; ++s)
-                    (void)mbar_wait_bounded(smem_addr(&ms->bar[s % p.stages]),
-                                            (uint32_t)((s / p.stages) & 1));
-            atomicOr(p.status, 1u);
-        }
-        n = 0;
-    }
+    if (ASYNC)
+        cp_async_wait_pending(0);
     __syncthreads();  // appends of the last stage are visible
 
     // -- final TopK of the slice ---------------------------------------------
@@ -596,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
 typedef void (*KernelFn)(Params);
 
 // Kernel entry points of one dtype, defined in ds_kernels_<dtype>.cu.
-KernelFn kernel_fp32(bool bulk, bool wide);
-KernelFn kernel_bf16(bool bulk, bool wide);
+KernelFn kernel_fp32(bool async, bool wide);
+KernelFn kernel_bf16(bool async, bool wide);
 
 }  // namespace ds

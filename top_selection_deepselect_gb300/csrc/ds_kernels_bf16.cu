@@ -3,9 +3,9 @@
 
 namespace ds {
 
-KernelFn kernel_bf16(bool bulk, bool wide)
+KernelFn kernel_bf16(bool async, bool wide)
 {
-    if (bulk)
+    if (async)
         return wide ? deepselect_topk_kernel<1, true, 16> : deepselect_topk_kernel<1, true, 4>;
     return wide ? deepselect_topk_kernel<1, false, 16> : deepselect_topk_kernel<1, false, 4>;
 }

@@ -3,9 +3,9 @@
 
 namespace ds {
 
-KernelFn kernel_fp32(bool bulk, bool wide)
+KernelFn kernel_fp32(bool async, bool wide)
 {
-    if (bulk)
+    if (async)
         return wide ? deepselect_topk_kernel<0, true, 16> : deepselect_topk_kernel<0, true, 4>;
     return wide ? deepselect_topk_kernel<0, false, 16> : deepselect_topk_kernel<0, false, 4>;
 }

@@ -14,11 +14,6 @@
 
 #include "ds_kernel.cuh"
 
-namespace ds {
-// Device status word: bit 0 = a kernel gave up waiting for a bulk copy.
-__device__ unsigned int g_status;
-}  // namespace ds
-
 // ===========================================================================
 // Host side: argument checks, launch planning, C ABI.
 // ===========================================================================
@@ -56,7 +51,6 @@ struct DevInfo {
     int smem_per_sm = 0;   // shared memory per SM
     int smem_reserved = 0; // reserved shared memory per CTA
     unsigned attr_set = 0; // kernels whose smem attribute was raised
-    unsigned int *status = nullptr;  // device address of the status word
 };
 
 constexpr int kMaxDevices = 64;
@@ -87,8 +81,6 @@ int device_info(DevInfo **out, int *dev_out)
         if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
             return fail_cuda(e, "cudaDeviceGetAttribute(reserved smem)");
         d.smem_reserved = v;
-        if ((e = cudaGetSymbolAddress((void **)&d.status, ds::g_status)) != cudaSuccess)
-            return fail_cuda(e, "cudaGetSymbolAddress(status)");
         d.ready = true;
     }
     *out = &d;
@@ -99,18 +91,18 @@ int device_info(DevInfo **out, int *dev_out)
 
 using ds::KernelFn;
 
-// 8 instantiations: dtype x bulk copies x mask rounds (4 rounds cover blocks
-// of up to 2 KiB per warp, 16 up to 8 KiB per warp).
-KernelFn kernel_for(int dtype, bool bulk, bool wide, int *slot)
+// 8 instantiations: dtype x asynchronous copies x mask rounds (4 rounds cover
+// blocks of up to 2 KiB per warp, 16 up to 8 KiB per warp).
+KernelFn kernel_for(int dtype, bool async, bool wide, int *slot)
 {
-    *slot = dtype * 4 + (bulk ? 2 : 0) + (wide ? 1 : 0);
-    return dtype == DS_FP32 ? ds::kernel_fp32(bulk, wide) : ds::kernel_bf16(bulk, wide);
+    *slot = dtype * 4 + (async ? 2 : 0) + (wide ? 1 : 0);
+    return dtype == DS_FP32 ? ds::kernel_fp32(async, wide) : ds::kernel_bf16(async, wide);
 }
 
-int ensure_attributes(DevInfo &d, int dtype, bool bulk, bool wide, KernelFn *fn)
+int ensure_attributes(DevInfo &d, int dtype, bool async, bool wide, KernelFn *fn)
 {
     int slot = 0;
-    *fn = kernel_for(dtype, bulk, wide, &slot);
+    *fn = kernel_for(dtype, async, wide, &slot);
     std::lock_guard<std::mutex> lock(g_mu);
     if (d.attr_set & (1u << slot))
         return DS_OK;
@@ -150,13 +142,13 @@ struct Plan {
     int grid;
     int smem;
     int ctas_per_sm;
-    bool bulk;
+    bool async;
 };
 
 
 // Shared-memory layout for a given split factor and ring depth.
 // Shared-memory layout for a given split factor and ring depth.  Every region
-// starts on a 128-byte boundary (bulk-copy destinations need 16 bytes, the
+// starts on a 128-byte boundary (asynchronous-copy destinations need 16 bytes, the
 // scratch words are read with 128-bit loads).
 long long align128(long long v) { return (v + 127) / 128 * 128; }
 
@@ -178,7 +170,7 @@ long long layout(Plan &pl, int stages, int splits)
     p.off_perm = (int)off;
     off = align128(off + (long long)ds::pow2_ceil((int)(per > 32 ? per : 32)) * 8);
     p.off_hist = (int)off;
-    off = align128(off + ds::kWarps * 256 * 4);
+    off = align128(off + ds::kHistWords * 4);
     p.off_holes = (int)off;
     off = align128(off + (long long)p.k * 2);
     p.off_misc = (int)off;
@@ -206,12 +198,13 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     const long long slot = ((long long)B * esz + 15) / 16 * 16;
     if (slot > 64 * 1024)
         return fail(DS_EUNSUPPORTED, "B * sizeof(elem) = %lld bytes exceeds 64 KiB", (long long)B * esz);
-    pl.bulk = ((uintptr_t)x % 16 == 0) && ((N * esz) % 16 == 0) && (((long long)B * esz) % 16 == 0);
+    pl.async = ((uintptr_t)x % 16 == 0) && ((N * esz) % 16 == 0) && (((long long)B * esz) % 16 == 0);
     p.slot_bytes = (int)slot;
     int wpb = 1;
     while (wpb < ds::kWarps && p.slot_bytes / (wpb * 2) >= 2048)
         wpb *= 2;
     p.wpb = wpb;
+    p.wpb_shift = wpb == 1 ? 0 : wpb == 2 ? 1 : wpb == 4 ? 2 : 3;
     p.bps = ds::kWarps / wpb;
     p.cpw = (p.slot_bytes / 16 + wpb - 1) / wpb;
 
@@ -232,7 +225,7 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     int splits = splits_req;
     if (splits == 0) {
         // aim for at least one CTA per SM when rows are few
-        const int stages_guess = pl.bulk ? 4 : 1;
+        const int stages_guess = pl.async ? 4 : 1;
         long long bytes1 = fits(stages_guess, 1, half_sm);
         int per_sm = bytes1 > 0 ? 2 : 1;
         const long long slots = (long long)d.sms * per_sm;
@@ -245,7 +238,7 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
                 want = m;
             splits = (int)(want < 1 ? 1 : want);
         }
-        while (splits > 1 && fits(pl.bulk ? 2 : 1, splits, budget_one) < 0)
+        while (splits > 1 && fits(pl.async ? 2 : 1, splits, budget_one) < 0)
             --splits;
     }
     if (splits > 1 && (long long)splits * k * 8 > budget_one)
@@ -260,7 +253,7 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     // ring depth: deepest that keeps two CTAs per SM, else deepest that fits
     int stages = 0;
     long long bytes = -1;
-    if (pl.bulk) {
+    if (pl.async) {
         for (int s = ds::kMaxStages; s >= 2 && bytes < 0; --s) {
             bytes = fits(s, splits, half_sm);
             if (bytes >= 0)
@@ -273,9 +266,9 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
         }
     }
     if (bytes < 0) {
-        // two bulk stages do not fit (or the layout forbids bulk copies):
+        // two ring slots do not fit (or the layout forbids 16-byte copies):
         // one stage filled by plain loads
-        pl.bulk = false;
+        pl.async = false;
         bytes = fits(1, splits, budget_one);
         stages = 1;
     }
@@ -348,7 +341,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     if ((rc = make_plan(x, dtype, rows, N, k, B, B2, splits_req, stats != nullptr, *d, pl)) != DS_OK)
         return rc;
     KernelFn fn = nullptr;
-    if ((rc = ensure_attributes(*d, dtype, pl.bulk, pl.p.cpw > 128, &fn)) != DS_OK)
+    if ((rc = ensure_attributes(*d, dtype, pl.async, pl.p.cpw > 128, &fn)) != DS_OK)
         return rc;
     // a cluster must fit on one GPC: shrink an automatic split factor until
     // the hardware can hold at least one cluster
@@ -375,7 +368,6 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     p.out_idx = out_idx;
     p.out_val = out_val;
     p.stats = reinterpret_cast<long long *>(stats);
-    p.status = d->status;
     p.seed_lo = (uint32_t)seed;
     p.seed_hi = (uint32_t)(seed >> 32);
 
@@ -486,7 +478,7 @@ int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, in
     plan->stages = pl.p.stages;
     plan->blocks_per_stage = pl.p.bps;
     plan->warps_per_block = pl.p.wpb;
-    plan->bulk = pl.bulk ? 1 : 0;
+    plan->async_copy = pl.async ? 1 : 0;
     plan->smem_bytes = pl.smem;
     plan->capacity = (pl.p.off_perm - pl.p.off_cand) / 8;
     plan->grid = pl.grid;
@@ -523,24 +515,6 @@ int ds_topk_max_k(int dtype, int B, int B2)
     return lo;
 }
 
-int ds_topk_device_status(void)
-{
-    g_detail[0] = '\0';
-    cudaError_t e = cudaDeviceSynchronize();
-    if (e != cudaSuccess)
-        return fail_cuda(e, "cudaDeviceSynchronize");
-    unsigned int v = 0, zero = 0;
-    e = cudaMemcpyFromSymbol(&v, ds::g_status, sizeof(v));
-    if (e != cudaSuccess)
-        return fail_cuda(e, "cudaMemcpyFromSymbol(status)");
-    e = cudaMemcpyToSymbol(ds::g_status, &zero, sizeof(zero));
-    if (e != cudaSuccess)
-        return fail_cuda(e, "cudaMemcpyToSymbol(status)");
-    if (v)
-        return fail(DS_EDEVICE, "a kernel gave up waiting for a bulk copy (status 0x%x)", v);
-    return DS_OK;
-}
-
 const char *ds_strerror(int status)
 {
     switch (status) {
@@ -548,7 +522,6 @@ const char *ds_strerror(int status)
     case DS_EINVAL: return "invalid argument";
     case DS_EUNSUPPORTED: return "unsupported dtype or working set too large for shared memory";
     case DS_ECUDA: return "CUDA runtime error";
-    case DS_EDEVICE: return "a kernel timed out waiting for a bulk copy";
     default: return "unknown status";
     }
 }
