@@ -156,6 +156,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_over_ranks(ms, rows, dist, device="cpu"):
+    """Slowest rank's time and the rows all ranks processed (weak scaling:
+    every rank runs its own batch; nothing but these two numbers is exchanged)."""
+    if dist is None:
+        return ms, rows
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    r = torch.tensor([rows], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(r, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(r.item())
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -317,10 +330,7 @@ def time_steps(torch, wl, steps, warmup, dist=None, burn_seconds=0.5):
     if dist is not None:
         dist.barrier()
     ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms, _ = reduce_over_ranks(ms, 0, dist, device="cuda")
     return ms
 
 
@@ -425,7 +435,8 @@ def run_ours(args, rank, world):
     clocks = sampler.stop() if sampler else None
 
     ms_per_step = ms / args.steps
-    value = world * wl.rows * args.steps / (ms * 1e-3)
+    _, total_rows = reduce_over_ranks(0.0, wl.rows * args.steps, dist, device="cuda")
+    value = total_rows / (ms * 1e-3)
     achieved = wl.read_bytes / (ms_per_step * 1e-3) / 1e9
     c = wl.c
     line = {
