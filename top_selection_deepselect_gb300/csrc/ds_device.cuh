@@ -440,10 +440,12 @@ struct Misc {
     unsigned long long tmin;             // select: smallest selected composite
 };
 
-// Per-warp 256-bin histograms of 16-bit counters, three rotating buffers.
-constexpr int kHistWordsPerWarp = 128;                     // 256 x u16
-constexpr int kHistBufWords = kWarps * kHistWordsPerWarp;  // one buffer
-constexpr int kHistWords = 3 * kHistBufWords;              // 12 KiB
+// Digit histograms: the register select uses one 256-bin histogram of 32-bit
+// counters per CTA, three rotating buffers; the shared-memory select uses one
+// per warp.  Both leave the region zero.
+constexpr int kHistBins = 256;
+constexpr int kHistWords = kWarps * kHistBins;  // 8 KiB
+static_assert(3 * kHistBins <= kHistWords, "rotating buffers fit the region");
 
 // Exclusive scan of one value per thread over the CTA (thread order).
 // Uses ms->wsum; ends synchronised.  Returns the exclusive prefix.
@@ -468,134 +470,133 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, Misc *ms)
 // threads; ends synchronised.
 //
 // Every thread loads its entries cand[tid + 256j] into registers once (up to
-// R of them); all passes then work on registers:
-//  1. OR and AND of all composites: only bits where they differ can separate
-//     entries, so digits start at the highest such bit and skip bits that
-//     never vary.
-//  2. Digit passes of 8 bits from the top: each warp builds its own 256-bin
-//     histogram of the entries still matching the chosen prefix with shared
-//     atomics (warps never contend); the CTA sums the eight histograms, scans
-//     them from the top bin down and picks the digit that holds the k-th
-//     entry.
-//  3. The loop stops when every entry matching the prefix is needed, or when
-//     at most 32 remain tied, which one warp ranks directly to find the exact
-//     k-th composite.
-//  4. Compaction: a CTA-wide scan of per-thread selected counts gives every
-//     selected entry its slot in cand[0, k); all entries are in registers, so
-//     the buffer is overwritten in place.
+// R of them), as two 32-bit halves; all passes then work on registers.  The
+// select is bound by issued instructions (every warp of the SM runs it), so
+// each step is kept to few instructions per entry:
+//  1. OR and AND of all composites (warp reductions): only bits where they
+//     differ can separate entries, so digits start at the highest such bit
+//     and skip bits that never vary.
+//  2. Digit passes of 8 bits from the top: every entry still matching the
+//     chosen prefix adds one to its bin of the CTA's 256-bin histogram (one
+//     shared atomic per entry); warp 0 then scans the histogram from the top
+//     bin down, finds the digit that holds the need-th entry and publishes it.
+//     Entries of higher digits are selected for good, those of other digits
+//     drop out.  Histogram buffers rotate over three, so clearing the next
+//     one needs no extra barrier.
+//  3. The loop stops when every entry of the chosen digit is needed, or when
+//     at most 32 remain tied; warp 0 then ranks the tied entries to find the
+//     exact k-th composite.
+//  4. Compaction: the selected entries of each register slot are counted by
+//     a warp ballot, one shared atomic per warp reserves their slots in
+//     cand[0, k), and the buffer is overwritten in place (all entries are in
+//     registers).
 // ---------------------------------------------------------------------------
-// One digit pass's decision, computed by every warp from the eight per-warp
-// histograms of buffer `hb` (16-bit counters, two per word): lane l owns
-// bins 8l .. 8l+7, lanes are scanned from the top bin down.  Returns the
-// digit holding the need-th entry, the count above it and its own count.
-__device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, int lane,
-                                             uint32_t &dsel, uint32_t &above, uint32_t &eq)
+// Warp 0's decision for one digit pass over histogram `hb`: lane l owns bins
+// 8l .. 8l+7; bins are ranked from the top.  Publishes the digit that holds
+// the need-th entry, the number of entries in higher bins and its own count.
+__device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, int lane, Misc *ms)
 {
-    uint32_t acc[4] = {0u, 0u, 0u, 0u};  // packed pairs of bin counts (no carry: n < 65536)
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(hb + w * kHistWordsPerWarp + lane * 4);
-        acc[0] += q.x;
-        acc[1] += q.y;
-        acc[2] += q.z;
-        acc[3] += q.w;
-    }
-    uint32_t c[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        c[2 * i] = acc[i] & 0xFFFFu;
-        c[2 * i + 1] = acc[i] >> 16;
-    }
-    uint32_t s = 0;
-#pragma unroll
-    for (int t = 0; t < 8; ++t)
-        s += c[t];
-    // suffix sum over lanes (lanes above hold higher bins)
-    uint32_t suf = s;
+    const uint4 q0 = *reinterpret_cast<const uint4 *>(hb + lane * 8);
+    const uint4 q1 = *reinterpret_cast<const uint4 *>(hb + lane * 8 + 4);
+    // cu_t: entries in this lane's bins 8l+7 down to 8l+t
+    const uint32_t cu7 = q1.w, cu6 = cu7 + q1.z, cu5 = cu6 + q1.y, cu4 = cu5 + q1.x;
+    const uint32_t cu3 = cu4 + q0.w, cu2 = cu3 + q0.z, cu1 = cu2 + q0.y, cu0 = cu1 + q0.x;
+    uint32_t suf = cu0;  // entries in the bins of this lane and all lanes above
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const uint32_t o = __shfl_down_sync(kFull, suf, d);
         if (lane + d < 32)
             suf += o;
     }
-    const uint32_t excl = suf - s;
-    uint32_t my_d = 0, my_above = 0, my_eq = 0;
+    const uint32_t excl = suf - cu0;
     const bool found = excl < need && need <= suf;
+    const uint32_t r = need - excl;
+    // bins of this lane lying wholly above the need-th entry
+    const uint32_t nb = (uint32_t)(cu7 < r) + (uint32_t)(cu6 < r) + (uint32_t)(cu5 < r) +
+                        (uint32_t)(cu4 < r) + (uint32_t)(cu3 < r) + (uint32_t)(cu2 < r) +
+                        (uint32_t)(cu1 < r);
+    const uint32_t before = nb == 0 ? 0u : nb == 1 ? cu7 : nb == 2 ? cu6 : nb == 3 ? cu5
+                          : nb == 4 ? cu4 : nb == 5 ? cu3 : nb == 6 ? cu2 : cu1;
+    const uint32_t through = nb == 0 ? cu7 : nb == 1 ? cu6 : nb == 2 ? cu5 : nb == 3 ? cu4
+                           : nb == 4 ? cu3 : nb == 5 ? cu2 : nb == 6 ? cu1 : cu0;
     if (found) {
-        uint32_t cum = excl;
-#pragma unroll
-        for (int t = 7; t >= 0; --t) {
-            if (my_eq == 0u && cum + c[t] >= need) {
-                my_d = (uint32_t)(8 * lane + t);
-                my_above = cum;
-                my_eq = c[t];
-            }
-            cum += c[t];
-        }
+        ms->sel_digit = 8u * (uint32_t)lane + 7u - nb;
+        ms->sel_above = excl + before;
+        ms->sel_eq = through - before;
     }
-    const int src = __ffs(__ballot_sync(kFull, found)) - 1;
-    dsel = __shfl_sync(kFull, my_d, src);
-    above = __shfl_sync(kFull, my_above, src);
-    eq = __shfl_sync(kFull, my_eq, src);
 }
 
-// ---------------------------------------------------------------------------
-// RadixSelectTopK ("算法", step 3) on n > k distinct composites in shared
-// memory.  After the call cand[0, k) holds the k largest (in no particular
-// order); returns the smallest of them, the new threshold.  Called by all
-// threads; ends synchronised.
-//
-// Every thread loads its entries cand[tid + 256j] into registers once (up to
-// R of them); all passes then work on registers:
-//  1. OR and AND of all composites: only bits where they differ can separate
-//     entries, so digits start at the highest such bit and skip bits that
-//     never vary.
-//  2. Digit passes of 8 bits from the top: each warp counts the entries that
-//     still match the chosen prefix into its own 256-bin histogram (shared
-//     atomics on 16-bit counters); after one barrier every warp sums the
-//     eight histograms and finds the digit holding the k-th entry by itself,
-//     so a pass costs a single barrier.  Buffers rotate over three so that a
-//     warp can clear the next one while others still read the last.
-//  3. The loop stops when every entry matching the prefix is needed, or when
-//     at most 32 remain tied; these are gathered and every warp ranks them
-//     to find the exact k-th composite.
-//  4. Compaction: each warp takes a run of slots in cand[0, k) with one
-//     shared atomic and its lanes fill it (positions from a warp scan); all
-//     entries are in registers, so the buffer is overwritten in place.
-// ---------------------------------------------------------------------------
+// Slots for the entries flagged in `bits` (bit j = register slot j) of all
+// lanes: one shared atomic per warp on *counter; returns the warp's base.
+__device__ __forceinline__ int warp_reserve(uint32_t bits, int *counter, int lane)
+{
+    uint32_t tot = 0u;
+    for (uint32_t m = __reduce_or_sync(kFull, bits); m; m &= m - 1u)
+        tot += (uint32_t)__popc(__ballot_sync(kFull, (bits >> (__ffs(m) - 1)) & 1u));
+    int base = 0;
+    if (lane == 0 && tot)
+        base = atomicAdd(counter, (int)tot);
+    return __shfl_sync(kFull, base, 0);
+}
+
+// Writes the flagged entries to dst[0, count): slot by slot, each lane's
+// position is the flagged lanes below it plus the earlier slots' totals.
+template <int R>
+__device__ __forceinline__ void warp_scatter(uint32_t bits, const uint32_t (&hi)[R],
+                                             const uint32_t (&lo)[R], unsigned long long *dst,
+                                             int lane)
+{
+    int run = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const uint32_t b = __ballot_sync(kFull, (bits >> j) & 1u);
+        if ((bits >> j) & 1u)
+            dst[run + __popc(b & lanemask_lt(lane))] = ((unsigned long long)hi[j] << 32) | lo[j];
+        run += __popc(b);
+    }
+}
+
 template <int R>
 static __device__ __noinline__ unsigned long long radix_select_regs(unsigned long long *cand, int n,
                                                                     int k, uint32_t *hist,
                                                                     Misc *ms)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    unsigned long long v[R];
+    uint32_t hi[R], lo[R], dg[R];
     uint32_t valid = 0u;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
         const int i = tid + kThreads * j;
-        v[j] = 0ull;
+        hi[j] = 0u;
+        lo[j] = 0u;
+        dg[j] = 0u;
         if (i < n) {
-            v[j] = cand[i];
+            const unsigned long long c = cand[i];
+            hi[j] = (uint32_t)(c >> 32);
+            lo[j] = (uint32_t)c;
             valid |= 1u << j;
         }
     }
     int pass = ms->pass;  // published before the previous barrier
 
     // 1. varying bits
-    unsigned long long vo = 0ull, va = ~0ull;
+    uint32_t oh = 0u, ol = 0u, ah = ~0u, al = ~0u;
 #pragma unroll
     for (int j = 0; j < R; ++j) {
         if (valid & (1u << j)) {
-            vo |= v[j];
-            va &= v[j];
+            oh |= hi[j];
+            ol |= lo[j];
+            ah &= hi[j];
+            al &= lo[j];
         }
     }
-    vo = warp_or_u64(vo);
-    va = warp_and_u64(va);
+    oh = __reduce_or_sync(kFull, oh);
+    ol = __reduce_or_sync(kFull, ol);
+    ah = __reduce_and_sync(kFull, ah);
+    al = __reduce_and_sync(kFull, al);
     if (lane == 0) {
-        ms->wor[warp] = vo;
-        ms->wand[warp] = va;
+        ms->wor[warp] = ((unsigned long long)oh << 32) | ol;
+        ms->wand[warp] = ((unsigned long long)ah << 32) | al;
     }
     __syncthreads();  // also: all loads of cand are done, every warp read ms->pass
     if (tid == 0) {
@@ -603,8 +604,7 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         ms->fill = 0;
         ms->tmin = ~0ull;
     }
-    vo = 0ull;
-    va = ~0ull;
+    unsigned long long vo = 0ull, va = ~0ull;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
         vo |= ms->wor[w];
@@ -613,97 +613,95 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
     const unsigned long long vary = vo ^ va;
 
     // 2./3. digit passes
-    unsigned long long prefix = 0ull, pmask = 0ull, texact = 0ull;
-    bool exact = false;
     uint32_t need = (uint32_t)k;
-    uint32_t live = valid;  // entries still matching the prefix
+    uint32_t live = valid;  // entries still matching the chosen prefix
+    uint32_t above = 0u;    // entries selected by a higher digit
+    bool exact = false;
+    unsigned long long texact = 0ull;
     int h = 63 - __clzll((long long)vary);
     while (true) {
-        const int lo = h >= 7 ? h - 7 : 0;
-        uint32_t *cur = hist + (pass % 3) * kHistBufWords;
-        uint32_t *nxt = hist + ((pass + 1) % 3) * kHistBufWords;
-        uint32_t *mine = cur + warp * kHistWordsPerWarp;
+        const int sh = h >= 7 ? h - 7 : 0;
+        uint32_t *cur = hist + (pass % 3) * kHistBins;
+        hist[((pass + 1) % 3) * kHistBins + tid] = 0u;
 #pragma unroll
-        for (int i = 0; i < kHistWordsPerWarp / 32; ++i)
-            nxt[warp * kHistWordsPerWarp + i * 32 + lane] = 0u;
+        for (int j = 0; j < R; ++j) {
+            const uint32_t d = (sh >= 32 ? hi[j] >> (sh - 32) : __funnelshift_r(lo[j], hi[j], sh)) & 255u;
+            dg[j] = d;
+            if (live & (1u << j))
+                atomicAdd(&cur[d], 1u);
+        }
+        __syncthreads();
+        if (warp == 0)
+            digit_search(cur, need, lane, ms);
+        __syncthreads();
+        const uint32_t dsel = ms->sel_digit, eq = ms->sel_eq;
+        need -= ms->sel_above;
+        ++pass;
 #pragma unroll
         for (int j = 0; j < R; ++j) {
             if (live & (1u << j)) {
-                const uint32_t d = (uint32_t)(v[j] >> lo) & 255u;
-                atomicAdd(&mine[d >> 1], 1u << ((d & 1u) << 4));
+                if (dg[j] > dsel)
+                    above |= 1u << j;
+                if (dg[j] != dsel)
+                    live &= ~(1u << j);
             }
         }
-        __syncthreads();
-        uint32_t dsel, above, eq;
-        digit_search(cur, need, lane, dsel, above, eq);
-        ++pass;
-        need -= above;
-        prefix |= (unsigned long long)dsel << lo;
-        pmask |= 255ull << lo;
-#pragma unroll
-        for (int j = 0; j < R; ++j)
-            if ((live & (1u << j)) && (((uint32_t)(v[j] >> lo) & 255u) != dsel))
-                live &= ~(1u << j);
         if (eq == need)
             break;
         if (eq <= 32u) {
-            // gather the tied entries, then every warp ranks them
-            const uint32_t cnt = (uint32_t)__popc(live);
-            const uint32_t incl = warp_inclusive_scan(cnt, lane);
-            int base = 0;
-            if (lane == 31 && incl)
-                base = atomicAdd(&ms->group_count, (int)incl);
-            base = __shfl_sync(kFull, base, 31);
-            int off = base + (int)(incl - cnt);
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-                if (live & (1u << j))
-                    ms->group[off++] = v[j];
+            // gather the tied entries; warp 0 ranks them
+            const int base = warp_reserve(live, &ms->group_count, lane);
+            warp_scatter<R>(live, hi, lo, ms->group + base, lane);
             __syncthreads();
-            const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
-            uint32_t rank = 0;
-            for (uint32_t j = 0; j < eq; ++j)
-                rank += ms->group[j] > g ? 1u : 0u;
-            const uint32_t bal = __ballot_sync(kFull, lane < (int)eq && rank == need - 1u);
-            texact = __shfl_sync(kFull, g, __ffs(bal) - 1);
+            if (warp == 0) {
+                const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
+                uint32_t rank = 0;
+                for (uint32_t j = 0; j < eq; ++j)
+                    rank += ms->group[j] > g ? 1u : 0u;
+                if (lane < (int)eq && rank == need - 1u)
+                    ms->texact = g;
+            }
+            __syncthreads();
+            texact = ms->texact;
             exact = true;
             break;
         }
         // eq > need >= 1 and composites are distinct: lower bits still vary
-        const unsigned long long below = lo > 0 ? (vary & ((1ull << lo) - 1ull)) : 0ull;
+        const unsigned long long below = sh > 0 ? (vary & ((1ull << sh) - 1ull)) : 0ull;
         if (below == 0ull)
             break;  // unreachable for distinct composites; keeps the loop finite
         h = 63 - __clzll((long long)below);
     }
 
     // 4. compaction
-    uint32_t sel = 0u;
-    unsigned long long mn = ~0ull;
+    uint32_t sel = above;
+    if (exact) {
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-        if (valid & (1u << j)) {
-            const bool s = exact ? (v[j] >= texact) : ((v[j] & pmask) >= prefix);
-            if (s) {
+        for (int j = 0; j < R; ++j)
+            if (((live >> j) & 1u) && (((unsigned long long)hi[j] << 32) | lo[j]) >= texact)
                 sel |= 1u << j;
-                mn = min_u64(mn, v[j]);
-            }
-        }
+    } else {
+        sel |= live;
     }
-    const uint32_t cnt = (uint32_t)__popc(sel);
-    const uint32_t incl = warp_inclusive_scan(cnt, lane);
-    int base = 0;
-    if (lane == 31 && incl)
-        base = atomicAdd(&ms->fill, (int)incl);
-    base = __shfl_sync(kFull, base, 31);
-    int pos = base + (int)(incl - cnt);
-#pragma unroll
-    for (int j = 0; j < R; ++j)
-        if (sel & (1u << j))
-            cand[pos++] = v[j];
+    warp_scatter<R>(sel, hi, lo, cand + warp_reserve(sel, &ms->fill, lane), lane);
     if (!exact) {
-        mn = warp_min_reduce(mn);
-        if (lane == 0 && mn != ~0ull)
-            atomicMin(&ms->tmin, mn);
+        // the chosen digit's entries are taken whole: the smallest of them
+        // is the k-th composite
+        uint32_t mh = ~0u, ml = ~0u;
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if ((live >> j) & 1u)
+                mh = min(mh, hi[j]);
+        mh = __reduce_min_sync(kFull, mh);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+            if (((live >> j) & 1u) && hi[j] == mh)
+                ml = min(ml, lo[j]);
+        ml = __reduce_min_sync(kFull, ml);
+        // (a NaN key is all ones, so the sentinel cannot tell whether a lane
+        // holds entries)
+        if (__any_sync(kFull, live != 0u) && lane == 0)
+            atomicMin(&ms->tmin, ((unsigned long long)mh << 32) | ml);
     }
     if (tid == 0)
         ms->pass = pass;
@@ -821,6 +819,8 @@ __device__ __forceinline__ unsigned long long radix_select_topk(unsigned long lo
                                                                 uint32_t *hist, uint16_t *holes,
                                                                 Misc *ms)
 {
+    if (n <= 4 * kThreads)
+        return radix_select_regs<4>(cand, n, k, hist, ms);
     if (n <= 8 * kThreads)
         return radix_select_regs<8>(cand, n, k, hist, ms);
     if (n <= 12 * kThreads)
