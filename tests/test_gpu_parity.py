@@ -150,6 +150,21 @@ def test_ties_and_special_values(dtype, kind):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("kind", ["normal", "specials", "levels", "ascending"])
+def test_split_rows_with_a_large_union(dtype, kind):
+    # splits * k above 8192: every slice sorts its own top k and CTA 0 merges
+    # the sorted runs pairwise (odd split counts carry a run to the next
+    # round); ragged rows leave some slices short or empty
+    bits, _ = workloads.generate(6, 60000, dtype, kind, seed=29, fraction=0.2, value=0.0)
+    row_len = np.array([60000, 0, 1500, 4095, 33333, 59999], dtype=np.int32)
+    for k, B, B2, splits in [(1100, 512, 512, 8), (1300, 1024, 256, 7), (2000, 512, 1024, 5),
+                             (4096, 1024, 1024, 3)]:
+        ref_idx, ref_val = oracle.topk(bits, dtype, k, row_len=row_len)
+        idx, val = run(bits, dtype, k, B, B2, row_len=row_len, splits=splits)
+        assert_same(idx, val, ref_idx, ref_val)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 def test_negative_zero_and_nan_bits_are_returned_as_read(dtype):
     f = np.zeros((4, 3000), dtype=np.float32)
     f[:, ::2] = -0.0

@@ -436,6 +436,7 @@ struct Misc {
     int merge_count;                     // CTA 0 of a cluster: entries received
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
     int fill;                            // select: slots handed out in the compaction
+    int runlen[16];                      // CTA 0 of a cluster: length of each slice's sorted run
     int pass;                            // select: digit passes so far (histogram rotation)
     unsigned long long tmin;             // select: smallest selected composite
 };

@@ -259,8 +259,15 @@ __device__ __forceinline__ void warp_append(const BlockView &bv, int lane, const
 // (the input is read again only for +-0 and NaN, whose keys do not determine
 // the bits).  Positions past cnt get index -1 and -inf.  Caller synchronises.
 // ---------------------------------------------------------------------------
+// Output pointers of the call and k (what the epilogue needs of Params).
+struct Out {
+    int32_t *idx;
+    void *val;
+    int k;
+};
+
 template <int DT>
-__device__ __forceinline__ void emit(const Params &p, long long obase, int pos,
+__device__ __forceinline__ void emit(const Out &p, long long obase, int pos,
                                      unsigned long long c, const unsigned char *xrow)
 {
     using E = Elem<DT>;
@@ -272,15 +279,15 @@ __device__ __forceinline__ void emit(const Params &p, long long obase, int pos,
                        : reinterpret_cast<const uint16_t *>(xrow)[idx];
     else
         bits = E::bits_of_key(key);
-    p.out_idx[obase + pos] = idx;
+    p.idx[obase + pos] = idx;
     if (DT == 0)
-        reinterpret_cast<uint32_t *>(p.out_val)[obase + pos] = bits;
+        reinterpret_cast<uint32_t *>(p.val)[obase + pos] = bits;
     else
-        reinterpret_cast<uint16_t *>(p.out_val)[obase + pos] = (uint16_t)bits;
+        reinterpret_cast<uint16_t *>(p.val)[obase + pos] = (uint16_t)bits;
 }
 
 template <int DT, int E>
-__device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, const Params &p,
+__device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, const Out &p,
                                           long long obase, const unsigned char *xrow)
 {
     const int P = 256 * E;
@@ -297,17 +304,17 @@ __device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, cons
 }
 
 template <int DT>
-__device__ void sort_and_write(unsigned long long *arr, int cnt, const Params &p, int row,
-                               const unsigned char *xrow)
+__device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt, const Out &p, int row,
+                                               const unsigned char *xrow)
 {
     using E = Elem<DT>;
     const long long obase = (long long)row * p.k;
     for (int i = cnt + threadIdx.x; i < p.k; i += kThreads) {
-        p.out_idx[obase + i] = -1;
+        p.idx[obase + i] = -1;
         if (DT == 0)
-            reinterpret_cast<uint32_t *>(p.out_val)[obase + i] = E::kNegInfBits;
+            reinterpret_cast<uint32_t *>(p.val)[obase + i] = E::kNegInfBits;
         else
-            reinterpret_cast<uint16_t *>(p.out_val)[obase + i] = (uint16_t)E::kNegInfBits;
+            reinterpret_cast<uint16_t *>(p.val)[obase + i] = (uint16_t)E::kNegInfBits;
     }
     if (cnt <= kThreads) {
         const int t = threadIdx.x;
@@ -333,6 +340,224 @@ __device__ void sort_and_write(unsigned long long *arr, int cnt, const Params &p
         for (int i = threadIdx.x; i < cnt; i += kThreads)
             emit<DT>(p, obase, i, arr[i], xrow);
     }
+}
+
+// Sorts the cnt distinct entries arr[0, cnt) descending, in place (the same
+// rank computations as sort_and_write; every entry moves to its rank).  arr
+// holds pow2_ceil(cnt) entries.  Caller synchronises before; ends
+// synchronised.
+template <int E>
+__device__ __forceinline__ void sort_runs_inplace(unsigned long long *arr, int cnt)
+{
+    for (int i = cnt + threadIdx.x; i < 256 * E; i += kThreads)
+        arr[i] = 0ull;
+    __syncthreads();
+    unsigned long long vals[E];
+    int ranks[E];
+    rank_desc_runs<E>(arr, vals, ranks);
+#pragma unroll
+    for (int j = 0; j < E; ++j)
+        if (vals[j] != 0ull)
+            arr[ranks[j]] = vals[j];
+    __syncthreads();
+}
+
+static __device__ __noinline__ void sort_desc_inplace(unsigned long long *arr, int cnt)
+{
+    if (cnt <= kThreads) {
+        const int t = threadIdx.x;
+        unsigned long long e = 0ull;
+        int rank = 0;
+        if (t < cnt) {
+            e = arr[t];
+            for (int j = 0; j < cnt; ++j)
+                rank += arr[j] > e ? 1 : 0;
+        }
+        __syncthreads();
+        if (t < cnt)
+            arr[rank] = e;
+        __syncthreads();
+    } else if (cnt <= 512) {
+        sort_runs_inplace<2>(arr, cnt);
+    } else if (cnt <= 1024) {
+        sort_runs_inplace<4>(arr, cnt);
+    } else if (cnt <= 2048) {
+        sort_runs_inplace<8>(arr, cnt);
+    } else {
+        const int P = pow2_ceil(cnt);
+        for (int i = cnt + threadIdx.x; i < P; i += kThreads)
+            arr[i] = 0ull;
+        __syncthreads();
+        bitonic_sort_smem(arr, P, true);
+    }
+}
+
+// Largest k for which CTA 0 merges the slices' sorted runs (every thread
+// holds at most kMergeOut outputs of a merge round in registers).
+constexpr int kMergeOut = 16;
+constexpr int kMergeMaxK = kThreads * kMergeOut;
+// Below this many entries in the union, CTA 0 selects from the union
+// directly (registers hold it) instead of merging sorted runs.
+constexpr int kMergeMinUnion = 8192;
+
+// Outputs [t0, t1) (at most kMergeOut) of the descending merge of runs A[0, la)
+// and B[0, lb): a merge-path search finds how many of the first t0 come from
+// A, then the two runs are walked.  Distinct nonzero entries; 0 pads.
+__device__ __forceinline__ void merge_chunk(const unsigned long long *A, int la,
+                                            const unsigned long long *B, int lb, int t0, int t1,
+                                            unsigned long long (&out)[kMergeOut])
+{
+    int lo = t0 - lb > 0 ? t0 - lb : 0, hi = t0 < la ? t0 : la;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > B[t0 - mid - 1])
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    int i = lo, j = t0 - lo;
+#pragma unroll
+    for (int q = 0; q < kMergeOut; ++q) {
+        if (q < t1 - t0) {
+            const unsigned long long a = i < la ? A[i] : 0ull;
+            const unsigned long long b = j < lb ? B[j] : 0ull;
+            const bool ta = a > b;
+            out[q] = ta ? a : b;
+            i += ta ? 1 : 0;
+            j += ta ? 0 : 1;
+        }
+    }
+}
+
+// CTA 0 of a split row: runs[s*k, s*k + ms->runlen[s]) holds slice s's top k
+// sorted descending.  Runs are merged pairwise, keeping the first k of each
+// merge (stride 1, 2, 4, ...: run s absorbs run s + stride), in place: each
+// round's outputs are held in registers across a barrier.  The last merge
+// writes the row's output directly.  Called by all threads of CTA 0.
+template <int DT>
+__device__ __forceinline__ void merge_runs_and_write(unsigned long long *runs, int S, const Out &p,
+                                                  int row, const unsigned char *xrow, Misc *ms)
+{
+    using E = Elem<DT>;
+    const int k = p.k, tid = threadIdx.x;
+    const long long obase = (long long)row * k;
+    for (int st = 1; st < S; st <<= 1) {
+        const bool last = 2 * st >= S;  // one pair left: (0, st)
+        int np = 0;                     // pairs (s, s + st), s = 2 st m, s + st < S
+        for (int s = 0; s + st < S; s += 2 * st)
+            ++np;
+        int G = 1;  // pairs per group: a power of two, at most kMergeOut outputs per thread
+        while (2 * G <= np && 2 * G * k <= kMergeMaxK)
+            G *= 2;
+        const int tpp = kThreads / G;
+        for (int g0 = 0; g0 < np; g0 += G) {
+            const int pair = g0 + tid / tpp, local = tid % tpp;
+            unsigned long long out[kMergeOut];
+            int s = 0, t0 = 0, t1 = 0, L = 0;
+            if (pair < np) {
+                s = pair * 2 * st;
+                const int la = ms->runlen[s], lb = ms->runlen[s + st];
+                L = la + lb < k ? la + lb : k;
+                const int chunk = (L + tpp - 1) / tpp;
+                t0 = local * chunk < L ? local * chunk : L;
+                t1 = t0 + chunk < L ? t0 + chunk : L;
+                if (t0 < t1)
+                    merge_chunk(runs + (size_t)s * k, la, runs + (size_t)(s + st) * k, lb, t0, t1, out);
+            }
+            if (last) {
+#pragma unroll
+                for (int q = 0; q < kMergeOut; ++q)
+                    if (q < t1 - t0)
+                        emit<DT>(p, obase, t0 + q, out[q], xrow);
+                for (int i = L + tid; i < k; i += kThreads) {
+                    p.idx[obase + i] = -1;
+                    if (DT == 0)
+                        reinterpret_cast<uint32_t *>(p.val)[obase + i] = E::kNegInfBits;
+                    else
+                        reinterpret_cast<uint16_t *>(p.val)[obase + i] = (uint16_t)E::kNegInfBits;
+                }
+                return;
+            }
+            __syncthreads();  // every read of this group's runs is done
+#pragma unroll
+            for (int q = 0; q < kMergeOut; ++q)
+                if (q < t1 - t0)
+                    runs[(size_t)s * k + t0 + q] = out[q];
+            if (pair < np && local == 0)
+                ms->runlen[s] = L;
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Epilogue of one slice: final TopK, counters, then the ordered output (one
+// CTA per row) or the cluster merge (split rows).  A separate function so
+// that the streaming loop is compiled on its own.  Called by all threads
+// after the scan; the candidate buffer holds n entries.
+// ---------------------------------------------------------------------------
+template <int DT>
+static __device__ __noinline__ void finish_slice(const Out o, long long *stats, unsigned char *ring,
+                                                 unsigned long long *cand, uint32_t *whist,
+                                                 uint16_t *holes, Misc *ms, int n, int S, int row,
+                                                 int slice, const unsigned char *xrow, int A, int R,
+                                                 int W, int peak)
+{
+    const int tid = threadIdx.x;
+    W += n;
+    if (n > o.k)
+        radix_select_topk(cand, n, o.k, whist, holes, ms);
+    const int cnt = n < o.k ? n : o.k;
+    if (stats != nullptr && tid == 0) {
+        long long *s = stats + ((long long)row * S + slice) * 4;
+        s[0] = A;
+        s[1] = R;
+        s[2] = W;
+        s[3] = peak;
+    }
+
+    if (S == 1) {
+        sort_and_write<DT>(cand, cnt, o, row, xrow);
+        return;
+    }
+
+    // -- split rows: partial top-k of every slice into CTA 0 -------------------
+    cg::cluster_group cluster = cg::this_cluster();
+    if (o.k <= kMergeMaxK && (long long)S * o.k > kMergeMinUnion) {
+        // a large union: each slice sorts its own top k, CTA 0 merges the
+        // sorted runs (cheaper than selecting from S*k entries in shared
+        // memory)
+        sort_desc_inplace(cand, cnt);
+        cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
+        unsigned long long *dst =
+            cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + (size_t)slice * o.k;
+        for (int i = tid; i < cnt; i += kThreads)
+            dst[i] = cand[i];
+        if (tid == 0)
+            *cluster.map_shared_rank(&ms->runlen[slice], 0) = cnt;
+        cluster.sync();
+        if (slice == 0)
+            merge_runs_and_write<DT>(reinterpret_cast<unsigned long long *>(ring), S, o, row, xrow, ms);
+        return;
+    }
+    // otherwise CTA 0 selects the top k of the union and orders it
+    cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
+    if (tid == 0)
+        ms->merge_off = atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), cnt);
+    __syncthreads();
+    unsigned long long *dst =
+        cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
+    for (int i = tid; i < cnt; i += kThreads)
+        dst[i] = cand[i];
+    cluster.sync();
+    if (slice != 0)
+        return;
+    const int total = ms->merge_count;
+    const int kk = total < o.k ? total : o.k;
+    unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
+    if (total > kk)
+        radix_select_topk(merged, total, kk, whist, holes, ms);
+    sort_and_write<DT>(merged, kk, o, row, xrow);
 }
 
 // ---------------------------------------------------------------------------
@@ -524,43 +749,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
         cp_async_wait_pending(0);
     __syncthreads();  // appends of the last stage are visible
 
-    // -- final TopK of the slice ---------------------------------------------
-    W += n;
-    if (n > p.k)
-        radix_select_topk(cand, n, p.k, whist, holes, ms);
-    const int cnt = n < p.k ? n : p.k;
-    if (p.stats != nullptr && tid == 0) {
-        long long *s = p.stats + ((long long)row * S + slice) * 4;
-        s[0] = A;
-        s[1] = R;
-        s[2] = W;
-        s[3] = peak;
-    }
-
-    if (S == 1) {
-        sort_and_write<DT>(cand, cnt, p, row, xrow);
-        return;
-    }
-
-    // -- split rows: partial top-k of every slice into CTA 0 -------------------
-    cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
-    if (tid == 0)
-        ms->merge_off = atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), cnt);
-    __syncthreads();
-    unsigned long long *dst =
-        cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
-    for (int i = tid; i < cnt; i += kThreads)
-        dst[i] = cand[i];
-    cluster.sync();
-    if (slice != 0)
-        return;
-    const int total = ms->merge_count;
-    const int kk = total < p.k ? total : p.k;
-    unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
-    if (total > kk)
-        radix_select_topk(merged, total, kk, whist, holes, ms);
-    sort_and_write<DT>(merged, kk, p, row, xrow);
+    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, p.stats, ring, cand, whist, holes, ms, n, S, row,
+                     slice, xrow, A, R, W, peak);
 }
 
 typedef void (*KernelFn)(Params);
