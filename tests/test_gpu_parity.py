@@ -293,3 +293,14 @@ def test_plans_of_the_workloads():
         assert plan["async_copy"] == 1
         assert plan["capacity"] >= c["k"] + c["B"] + c["B2"]
         assert plan["grid"] == c["rows"] * plan["splits"]
+        s = plan["splits"]
+        assert s & (s - 1) == 0 and s <= 16
+        # one wave: at most the resident CTAs of the device
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert plan["grid"] <= sms * plan["ctas_per_sm"]
+        if sms == 152:
+            # short rows: one CTA per SM; long rows: two per SM
+            want = {"small_fp32": 16, "dsa_index_bf16": 2, "sampling_logits_bf16": 1,
+                    "adversarial_fp32": 8}
+            if name in want:
+                assert s == want[name], (name, plan)

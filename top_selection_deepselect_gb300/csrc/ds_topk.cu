@@ -179,6 +179,8 @@ long long layout(Plan &pl, int stages, int splits)
 }
 
 constexpr long long kMaxPermBlocks = 4096;  // blocks per slice the in-CTA order holds
+constexpr long long kMaxAutoSplits = 16;     // largest automatic split factor
+constexpr long long kStreamSliceBytes = 128 * 1024;  // slices that keep a second CTA per SM busy
 
 int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits_req,
               bool stats, DevInfo &d, Plan &pl)
@@ -221,25 +223,33 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
         return bytes <= limit ? bytes : -1;
     };
 
-    // split factor
+    // split factor (automatic): a power of two, at most kMaxAutoSplits and
+    // one block per slice.  Rows that are short for the GPU run latency
+    // bound, and two CTAs on one SM slow each other down, so the default
+    // fills the SMs with one CTA each; a second CTA per SM is taken only
+    // when its slices still stream at least kStreamSliceBytes each.
     int splits = splits_req;
     if (splits == 0) {
-        // aim for at least one CTA per SM when rows are few
-        const int stages_guess = pl.async ? 4 : 1;
-        long long bytes1 = fits(stages_guess, 1, half_sm);
-        int per_sm = bytes1 > 0 ? 2 : 1;
-        const long long slots = (long long)d.sms * per_sm;
-        splits = 1;
-        if ((long long)rows * 2 < slots) {
-            long long want = slots / (rows > 0 ? rows : 1);
-            if (want > 8)
-                want = 8;
-            if (want > m)
-                want = m;
-            splits = (int)(want < 1 ? 1 : want);
-        }
-        while (splits > 1 && fits(pl.async ? 2 : 1, splits, budget_one) < 0)
-            --splits;
+        const long long r = rows > 0 ? rows : 1;
+        auto pow2_floor = [](long long v) {
+            long long q = 1;
+            while (2 * q <= v)
+                q *= 2;
+            return q;
+        };
+        auto cap = [&](long long v) {
+            v = v < kMaxAutoSplits ? v : kMaxAutoSplits;
+            v = v < m ? v : m;
+            return pow2_floor(v < 1 ? 1 : v);
+        };
+        long long one = cap((long long)d.sms / r);
+        while (one > 1 && fits(pl.async ? 2 : 1, (int)one, budget_one) < 0)
+            one /= 2;
+        long long two = cap(2LL * d.sms / r);
+        while (two > one && fits(pl.async ? 2 : 1, (int)two, half_sm) < 0)
+            two /= 2;
+        const long long slice_bytes = (m + two - 1) / two * (long long)B * esz;
+        splits = (int)(two > one && slice_bytes >= kStreamSliceBytes ? two : one);
     }
     if (splits > 1 && (long long)splits * k * 8 > budget_one)
         return fail(DS_EUNSUPPORTED, "splits * k * 8 = %lld bytes does not fit shared memory",
@@ -356,7 +366,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
                         "a cluster of %d CTAs with %d bytes of shared memory each cannot be "
                         "scheduled on this device",
                         pl.p.splits, pl.smem);
-        if ((rc = make_plan(x, dtype, rows, N, k, B, B2, pl.p.splits - 1, stats != nullptr, *d,
+        if ((rc = make_plan(x, dtype, rows, N, k, B, B2, pl.p.splits / 2, stats != nullptr, *d,
                             pl)) != DS_OK)
             return rc;
     }
