@@ -35,7 +35,8 @@ _LIB_PATH = os.path.join(_HERE, "libds_oracle.so")
 
 FP32 = 0
 BF16 = 1
-_DTYPE_CODES = {"fp32": FP32, "bf16": BF16, FP32: FP32, BF16: BF16}
+FP16 = 2
+_DTYPE_CODES = {"fp32": FP32, "bf16": BF16, "fp16": FP16, FP32: FP32, BF16: BF16, FP16: FP16}
 
 _lock = threading.Lock()
 _lib = None
@@ -60,6 +61,8 @@ def _bind(lib):
     lib.ds_oracle_key_f32.restype = ctypes.c_uint32
     lib.ds_oracle_key_bf16.argtypes = [ctypes.c_uint32]
     lib.ds_oracle_key_bf16.restype = ctypes.c_uint32
+    lib.ds_oracle_key_f16.argtypes = [ctypes.c_uint32]
+    lib.ds_oracle_key_f16.restype = ctypes.c_uint32
     lib.ds_oracle_keys.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, c_u32p]
     lib.ds_oracle_keys.restype = None
     lib.ds_oracle_topk.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, c_i32p,
@@ -95,12 +98,14 @@ def _ptr(a, ctype):
 
 
 def _as_bits(x, dtype):
-    """x as a C-contiguous array of raw bit patterns (uint32 for fp32, uint16 for bf16)."""
+    """x as a C-contiguous array of raw bit patterns (uint32 for fp32, uint16 for bf16 / fp16)."""
     code = _DTYPE_CODES[dtype]
     want = np.uint32 if code == FP32 else np.uint16
     a = np.asarray(x)
     if a.dtype == np.float32 and code == FP32:
         a = a.view(np.uint32)
+    if a.dtype == np.float16 and code == FP16:
+        a = a.view(np.uint16)
     if a.dtype != want:
         raise TypeError("expected %s bit patterns, got %s" % (want, a.dtype))
     return np.ascontiguousarray(a), code

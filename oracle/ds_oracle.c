@@ -14,7 +14,8 @@
  *         (expected-work bound: A, R, W, W = A + kR, R*B2 <= A).
  *   [OPS] milkfeng.top "CUDA 算子笔记 4" -- section "Top K Selection"
  *         (problem statement and worked example) and its sub-section
- *         "改造 Radix Sort" (order-preserving float -> unsigned key map).
+ *         "改造 Radix Sort" (order-preserving float -> unsigned key map; the
+ *         same construction serves fp32, bf16 and IEEE binary16).
  *   [PHX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
  *         1, 2, 3", SC'11 -- definition of Philox4x32-10.
  *
@@ -54,6 +55,7 @@
 
 #define DS_ORACLE_FP32 0
 #define DS_ORACLE_BF16 1
+#define DS_ORACLE_FP16 2
 
 /* ------------------------------------------------------------------------ */
 /* Total order: unsigned key whose order is the value order.                 */
@@ -87,6 +89,26 @@ uint32_t ds_oracle_key_bf16(uint32_t bits16)
     return bits | 0x8000u;
 }
 
+/* IEEE binary16: 5 exponent bits, 10 mantissa bits; the infinity pattern
+ * is 0x7C00 and every larger magnitude is a NaN. */
+uint32_t ds_oracle_key_f16(uint32_t bits16)
+{
+    uint32_t bits = bits16 & 0xFFFFu;
+    uint32_t magnitude = bits & 0x7FFFu;
+    if (magnitude > 0x7C00u)
+        return 0xFFFFu;
+    if (magnitude == 0u)
+        return 0x8000u;
+    if (bits & 0x8000u)
+        return (~bits) & 0xFFFFu;
+    return bits | 0x8000u;
+}
+
+static int dtype_known(int dtype)
+{
+    return dtype == DS_ORACLE_FP32 || dtype == DS_ORACLE_BF16 || dtype == DS_ORACLE_FP16;
+}
+
 static uint32_t element_bits(const void *x, int dtype, int64_t pos)
 {
     if (dtype == DS_ORACLE_FP32)
@@ -97,7 +119,9 @@ static uint32_t element_bits(const void *x, int dtype, int64_t pos)
 static uint32_t element_key(const void *x, int dtype, int64_t pos)
 {
     uint32_t bits = element_bits(x, dtype, pos);
-    return dtype == DS_ORACLE_FP32 ? ds_oracle_key_f32(bits) : ds_oracle_key_bf16(bits);
+    if (dtype == DS_ORACLE_FP32)
+        return ds_oracle_key_f32(bits);
+    return dtype == DS_ORACLE_BF16 ? ds_oracle_key_bf16(bits) : ds_oracle_key_f16(bits);
 }
 
 /* Keys of n elements, for the tests. */
@@ -145,7 +169,8 @@ static void write_output(const void *x, int dtype, int64_t row_base, const pair_
 {
     for (int64_t i = 0; i < k; ++i) {
         int32_t idx = -1;
-        uint32_t bits = dtype == DS_ORACLE_FP32 ? 0xFF800000u : 0xFF80u; /* -inf */
+        uint32_t bits = dtype == DS_ORACLE_FP32 ? 0xFF800000u
+                      : dtype == DS_ORACLE_BF16 ? 0xFF80u : 0xFC00u; /* -inf */
         if (i < count) {
             idx = sorted[i].idx;
             bits = element_bits(x, dtype, row_base + idx);
@@ -167,7 +192,7 @@ static void write_output(const void *x, int dtype, int64_t row_base, const pair_
 int ds_oracle_topk(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N,
                    int k, int32_t *out_idx, void *out_val)
 {
-    if (rows < 0 || N < 1 || k < 1 || (dtype != DS_ORACLE_FP32 && dtype != DS_ORACLE_BF16))
+    if (rows < 0 || N < 1 || k < 1 || !dtype_known(dtype))
         return -1;
     pair_t *pairs = (pair_t *)malloc((size_t)N * sizeof(pair_t));
     if (!pairs)
@@ -291,7 +316,7 @@ int ds_oracle_model(const void *x, int dtype, int rows, const int32_t *row_len, 
                     int32_t *out_idx, void *out_val, int64_t *stats)
 {
     if (rows < 0 || N < 1 || k < 1 || B < 1 || B2 < 1 || splits < 1 ||
-        (dtype != DS_ORACLE_FP32 && dtype != DS_ORACLE_BF16))
+        !dtype_known(dtype))
         return -1;
     int64_t m_max = (N + B - 1) / B;
     pair_t *cand = (pair_t *)malloc((size_t)(N + 1) * sizeof(pair_t));

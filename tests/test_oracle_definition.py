@@ -23,6 +23,7 @@ import workloads
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 NEG_INF_F32 = np.uint32(0xFF800000)
 NEG_INF_BF16 = np.uint16(0xFF80)
+NEG_INF_F16 = np.uint16(0xFC00)
 
 
 def _read_golden(name):
@@ -96,12 +97,13 @@ def _vectorised_ranks(f):
     return before.sum(axis=1)  # [rows, n]: rank of element i
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6])
 def test_bruteforce_exhaustive_specials(dtype, n):
     combos = np.array(list(itertools.product(range(len(ALPHABET)), repeat=n)), dtype=np.int64)
     f = np.array(ALPHABET, dtype=np.float32)[combos]
-    bits = f.view(np.uint32) if dtype == "fp32" else workloads.to_bf16_bits(f)
+    bits = f.view(np.uint32) if dtype == "fp32" else \
+        workloads.to_bf16_bits(f) if dtype == "bf16" else workloads.to_f16_bits(f)
     ranks = _vectorised_ranks(f)
     expected_order = np.argsort(ranks, axis=1)   # ranks are a permutation of 0..n-1
     for k in sorted({1, (n + 1) // 2, n}):
@@ -136,7 +138,7 @@ def test_bruteforce_random_longer_rows():
 # ---------------------------------------------------------------------------
 # Closed forms and library routines.
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_k_equals_len_is_full_stable_descending_sort(dtype):
     bits, _ = workloads.generate(6, 3000, dtype, "normal", seed=3)
     f = workloads.bits_to_f32(bits, dtype)
@@ -156,7 +158,7 @@ def test_k1_is_argmax_lowest_index_nan_first():
     np.testing.assert_array_equal(val[:, 0], bits[np.arange(64), idx[:, 0]])
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_constant_row_gives_first_k_indices(dtype):
     bits, _ = workloads.generate(3, 1000, dtype, "constant", seed=0, value=-3.5)
     idx, val = oracle.topk(bits, dtype, 77)
@@ -172,7 +174,7 @@ def test_ascending_distinct_row_gives_last_indices():
     np.testing.assert_array_equal(idx, np.tile(np.arange(4999, 4699, -1), (4, 1)))
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_few_levels_take_lowest_indices_of_top_levels(dtype):
     bits, _ = workloads.generate(5, 4000, dtype, "levels", seed=9, levels=16)
     f = workloads.bits_to_f32(bits, dtype)
@@ -183,13 +185,13 @@ def test_few_levels_take_lowest_indices_of_top_levels(dtype):
         np.testing.assert_array_equal(idx[r], expected)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_row_len_padding_and_clamping(dtype):
     bits, _ = workloads.generate(5, 64, dtype, "normal", seed=12)
     row_len = np.array([0, 3, 64, 1000, -5], dtype=np.int32)
     idx, val = oracle.topk(bits, dtype, 10, row_len=row_len)
     full_idx, _ = oracle.topk(bits, dtype, 10)
-    pad = NEG_INF_F32 if dtype == "fp32" else NEG_INF_BF16
+    pad = {"fp32": NEG_INF_F32, "bf16": NEG_INF_BF16, "fp16": NEG_INF_F16}[dtype]
     assert (idx[0] == -1).all() and (val[0] == pad).all()
     short_idx, _ = oracle.topk(bits[1:2, :3], dtype, 3)
     np.testing.assert_array_equal(idx[1, :3], short_idx[0])
@@ -199,7 +201,7 @@ def test_row_len_padding_and_clamping(dtype):
     assert (idx[4] == -1).all()                                  # negative -> empty
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_output_invariants_random(dtype):
     bits, row_len = workloads.generate(12, 4096, dtype, "ragged_normal", seed=21, min_len=100)
     k = 256
@@ -247,6 +249,31 @@ def test_bf16_key_map_exhaustive():
         eq_val = (fs[:-1] == fs[1:]) | (np.isnan(fs[:-1]) & np.isnan(fs[1:]))
     np.testing.assert_array_equal(same, eq_val)
     # bf16 keys agree with fp32 keys of the exact widening
+    k32 = oracle.keys(f.view(np.uint32), "fp32")
+    np.testing.assert_array_equal(np.argsort(k, kind="stable"), np.argsort(k32, kind="stable"))
+
+
+def test_fp16_key_map_exhaustive():
+    # every IEEE binary16 pattern, ordered by key, is ordered by value (numpy
+    # float16 compares), and keys are equal exactly for equal values
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f = workloads.bits_to_f32(bits, "fp16")
+    np.testing.assert_array_equal(f, bits.view(np.float16).astype(np.float32))
+    k = oracle.keys(bits, "fp16")
+    assert k.max() <= 0xFFFF
+    order = np.argsort(k, kind="stable")
+    h = bits.view(np.float16)[order]
+    a, b = h[:-1], h[1:]
+    na, nb = np.isnan(a), np.isnan(b)
+    with np.errstate(invalid="ignore"):
+        assert ((nb & ~na) | (na & nb) | (~na & ~nb & (a <= b))).all()
+        same = k[order][:-1] == k[order][1:]
+        np.testing.assert_array_equal(same, (a == b) | (na & nb))
+    # the boundaries: +inf is the largest non-NaN key, -0 and +0 share a key
+    inf_key = oracle.keys(np.array([0x7C00], np.uint16), "fp16")[0]
+    assert inf_key == k[~np.isnan(bits.view(np.float16))].max()
+    assert oracle.keys(np.array([0x8000, 0x0000], np.uint16), "fp16").tolist() == [0x8000, 0x8000]
+    # fp16 keys order the values exactly as fp32 keys of the widening do
     k32 = oracle.keys(f.view(np.uint32), "fp32")
     np.testing.assert_array_equal(np.argsort(k, kind="stable"), np.argsort(k32, kind="stable"))
 

@@ -60,7 +60,7 @@ def test_model_split_rows_match_definition(splits):
     assert stats.shape == (6, splits, 4)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("kind", ["levels", "specials", "constant", "ascending"])
 def test_model_matches_definition_with_ties_and_specials(dtype, kind):
     bits, _ = workloads.generate(4, 9000, dtype, kind, seed=41)

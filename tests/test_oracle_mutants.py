@@ -29,7 +29,9 @@ MUTANTS = {
     "nan_not_canonical": ("    if (magnitude > 0x7F800000u)      /* NaN, any sign or payload */\n"
                           "        return 0xFFFFFFFFu;\n", ""),
     "negative_not_flipped": ("        return ~bits;\n", "        return bits;\n"),
-    "bf16_sign_bit_wrong": ("    return bits | 0x8000u;", "    return bits | 0x4000u;"),
+    "bf16_sign_bit_wrong": ("        return 0xFFFFu;\n    if (magnitude == 0u)\n        return 0x8000u;\n    if (bits & 0x8000u)\n        return (~bits) & 0xFFFFu;\n    return bits | 0x8000u;\n}\n\n/* IEEE",
+                            "        return 0xFFFFu;\n    if (magnitude == 0u)\n        return 0x8000u;\n    if (bits & 0x8000u)\n        return (~bits) & 0xFFFFu;\n    return bits | 0x4000u;\n}\n\n/* IEEE"),
+    "fp16_inf_taken_as_nan": ("    if (magnitude > 0x7C00u)\n", "    if (magnitude >= 0x7C00u)\n"),
     "row_len_not_clamped": ("    if (len > N)\n        len = N;\n", ""),
     "threshold_is_largest": ("threshold = cand[n - 1];", "threshold = cand[0];"),
     "filter_operands_swapped": ("pair_before(p, threshold)", "pair_before(threshold, p)"),
@@ -78,8 +80,9 @@ def _battery(lib):
     combos = np.array(list(itertools.product(range(len(SPECIALS)), repeat=4)))
     f = np.array(SPECIALS, dtype=np.float32)[combos]
     order = _brute_order(f)
-    for dt in ["fp32", "bf16"]:
-        bits = f.view(np.uint32) if dt == "fp32" else workloads.to_bf16_bits(f)
+    for dt in ["fp32", "bf16", "fp16"]:
+        bits = f.view(np.uint32) if dt == "fp32" else \
+            workloads.to_bf16_bits(f) if dt == "bf16" else workloads.to_f16_bits(f)
         check("brute_force_" + dt,
               lambda b=bits, d=dt: np.array_equal(oracle.topk(b, d, 2, lib=lib)[0], order[:, :2]))
 

@@ -18,6 +18,7 @@ import numpy as np
 
 FP32 = "fp32"
 BF16 = "bf16"
+FP16 = "fp16"
 
 # name -> shape, dtype, selection parameters, value recipe and data seed
 CONFIGS = {
@@ -53,16 +54,25 @@ def to_bf16_bits(f32):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def to_f16_bits(f32):
+    """IEEE binary16 bit patterns of float32 values (round to nearest even)."""
+    return np.ascontiguousarray(np.asarray(f32, dtype=np.float32).astype(np.float16)).view(np.uint16)
+
+
 def bits_to_f32(bits, dtype):
-    """Widen bit patterns to float32 values (exact for bf16)."""
+    """Widen bit patterns to float32 values (exact for bf16 and fp16)."""
     if dtype == FP32:
         return np.asarray(bits, dtype=np.uint32).view(np.float32)
+    if dtype == FP16:
+        return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
 def _finish(f32, dtype):
     if dtype == FP32:
         return np.ascontiguousarray(f32, dtype=np.float32).view(np.uint32)
+    if dtype == FP16:
+        return to_f16_bits(f32)
     return to_bf16_bits(f32)
 
 
@@ -127,7 +137,14 @@ def generate(rows, N, dtype, kind, seed, **kw):
         bits[nan_mask] = (bits[nan_mask] & np.uint32(0xFFC00000)) | payload
     else:
         raise ValueError("unknown kind %r" % kind)
-    return _finish(f, dtype), row_len
+    out = _finish(f, dtype)
+    if kind == "specials" and dtype == FP16:
+        # the narrowing canonicalises NaNs: give them distinct 10-bit payloads
+        nan16 = (out & np.uint16(0x7C00)) == np.uint16(0x7C00)
+        nan16 &= (out & np.uint16(0x03FF)) != 0
+        pl = rng.integers(1, 1 << 10, size=int(nan16.sum()), dtype=np.uint32).astype(np.uint16)
+        out[nan16] = (out[nan16] & np.uint16(0xFC00)) | pl
+    return out, row_len
 
 
 def config_inputs(name, rows=None):
