@@ -3,7 +3,7 @@
  *
  * Operation (PFCCLab/DeepSelect "DeepSelect-deep-dive", section "算法", and
  * milkfeng.top "CUDA 算子笔记 4", section "Top K Selection"): for every row r
- * of a [rows x N] score matrix, return the k largest of its first row_len[r]
+ * of a [rows x N] score matrix (fp32, bf16 or IEEE fp16), return the k largest of its first row_len[r]
  * elements and their indices.  The result is exact and unique:
  *   - order: value descending; NaN (any payload) above +inf; -0.0 == +0.0;
  *     equal values by lower index first;
@@ -53,6 +53,7 @@ extern "C" {
 
 #define DS_FP32 0
 #define DS_BF16 1
+#define DS_FP16 2 /* IEEE binary16; the same key order (NaN above +inf, -0 == +0) */
 
 /* Launch plan chosen for a call (filled by ds_topk_plan). */
 typedef struct {
@@ -70,7 +71,7 @@ typedef struct {
 
 /*
  * ds_topk -- top-k of every row, sorted by (value desc, index asc).
- *   x        device, [rows][N] elements of `dtype` (DS_FP32 or DS_BF16)
+ *   x        device, [rows][N] elements of `dtype` (DS_FP32, DS_BF16 or DS_FP16)
  *   rows     >= 0 (0 is a no-op)
  *   row_len  device int32[rows] valid lengths, or NULL for N in every row
  *   N        row pitch and maximum length, 1 <= N < 2^31

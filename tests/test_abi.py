@@ -42,6 +42,13 @@ def test_library_is_built_for_sm_103a(lib):
     assert "--use_fast_math" not in _build.NVCC_FLAGS
 
 
+def test_dtype_codes():
+    # fp32, bf16 and IEEE fp16 are the dtypes of include/ds_topk.h
+    assert (ds.DS_FP32, ds.DS_BF16, ds.DS_FP16) == (0, 1, 2)
+    text = open(HEADER).read()
+    assert "#define DS_FP16 2" in text
+
+
 def test_strerror_texts(lib):
     for status in [ds.DS_OK, ds.DS_EINVAL, ds.DS_EUNSUPPORTED, ds.DS_ECUDA]:
         assert ds.ds_strerror(status)
@@ -53,6 +60,7 @@ FAKE = 1 << 20  # never dereferenced: these calls fail their checks first
 
 @pytest.mark.parametrize("args,status", [
     (dict(dtype=7), ds.DS_EUNSUPPORTED),
+    (dict(dtype=3), ds.DS_EUNSUPPORTED),
     (dict(rows=-1), ds.DS_EINVAL),
     (dict(N=0), ds.DS_EINVAL),
     (dict(N=1 << 31), ds.DS_EINVAL),

@@ -39,13 +39,22 @@ SEED = 0x5EED5EED
 def to_device(bits, dtype):
     if dtype == "fp32":
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int32)).to(DEV).view(torch.float32)
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(torch.bfloat16)
+    t16 = torch.bfloat16 if dtype == "bf16" else torch.float16
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(DEV).view(t16)
 
 
 def val_bits(t, dtype):
     if dtype == "fp32":
         return t.view(torch.int32).cpu().numpy().view(np.uint32)
     return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def float_bits(f, dtype):
+    """Bit patterns of float32 values in `dtype` (round to nearest even)."""
+    f = np.ascontiguousarray(f, dtype=np.float32)
+    if dtype == "fp32":
+        return f.view(np.uint32).copy()
+    return workloads.to_bf16_bits(f) if dtype == "bf16" else workloads.to_f16_bits(f)
 
 
 def run(bits, dtype, k, B, B2, seed=SEED, row_len=None, splits=0, stats=False):
@@ -133,7 +142,7 @@ def test_stats_match_model(name, splits):
 # ---------------------------------------------------------------------------
 # Edge cases.
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("kind", ["specials", "levels", "constant", "ascending"])
 def test_ties_and_special_values(dtype, kind):
     bits, _ = workloads.generate(16, 20000, dtype, kind, seed=17, fraction=0.2, value=0.0)
@@ -149,7 +158,7 @@ def test_ties_and_special_values(dtype, kind):
     assert_same(idx, val, ref_idx, ref_val)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("kind", ["normal", "specials", "levels", "ascending"])
 def test_split_rows_with_a_large_union(dtype, kind):
     # splits * k above 8192: every slice sorts its own top k and CTA 0 merges
@@ -164,7 +173,19 @@ def test_split_rows_with_a_large_union(dtype, kind):
         assert_same(idx, val, ref_idx, ref_val)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("kind,rows,N,k,B,B2", [("normal", 64, 32768, 512, 1024, 1024),
+                                                ("gumbel_spikes", 16, 128000, 50, 1024, 1024),
+                                                ("adversarial", 8, 65536, 1024, 1024, 1024)])
+@pytest.mark.parametrize("splits", [0, 1])
+def test_fp16_workload_shapes(kind, rows, N, k, B, B2, splits):
+    # the DSA index, sampling and adversarial shapes with IEEE fp16 inputs
+    bits, _ = workloads.generate(rows, N, "fp16", kind, seed=31)
+    ref_idx, ref_val = oracle.topk(bits, "fp16", k)
+    idx, val = run(bits, "fp16", k, B, B2, splits=splits)
+    assert_same(idx, val, ref_idx, ref_val)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_negative_zero_and_nan_bits_are_returned_as_read(dtype):
     f = np.zeros((4, 3000), dtype=np.float32)
     f[:, ::2] = -0.0
@@ -172,17 +193,20 @@ def test_negative_zero_and_nan_bits_are_returned_as_read(dtype):
     f[2, 5] = -np.inf
     f[3, :] = -1.0
     f[3, 2999] = -0.0
-    bits = f.view(np.uint32).copy() if dtype == "fp32" else workloads.to_bf16_bits(f)
+    bits = float_bits(f, dtype)
     if dtype == "fp32":
         bits[1, 100:110] |= np.arange(1, 11, dtype=np.uint32)      # NaN payloads
         bits[1, 105] |= np.uint32(0x80000000)                      # a negative NaN
+    if dtype == "fp16":
+        bits[1, 100:110] = np.uint16(0x7C00) | np.arange(1, 11, dtype=np.uint16)
+        bits[1, 105] |= np.uint16(0x8000)
     for k in [1, 17, 64]:
         ref_idx, ref_val = oracle.topk(bits, dtype, k)
         idx, val = run(bits, dtype, k, 128, 128, splits=1)
         assert_same(idx, val, ref_idx, ref_val)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_row_len_edges(dtype):
     bits, _ = workloads.generate(8, 4096, dtype, "normal", seed=23)
     row_len = np.array([0, 1, 63, 64, 65, 4096, 100000, -7], dtype=np.int32)
@@ -192,7 +216,7 @@ def test_row_len_edges(dtype):
         assert_same(idx, val, ref_idx, ref_val)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("N,k,B,B2", [(1, 1, 1, 1), (7, 3, 1, 1), (1000, 1000, 100, 3),
                                       (4099, 13, 100, 50), (3001, 200, 1000, 17),
                                       (65536, 64, 16384, 512), (20000, 2048, 64, 4000)])
@@ -205,7 +229,7 @@ def test_shapes_block_sizes_and_plain_load_path(dtype, N, k, B, B2):
         assert_same(idx, val, ref_idx, ref_val)
 
 
-@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_misaligned_input_pointer(dtype):
     rows, N, k = 6, 8192, 100
     bits, _ = workloads.generate(rows, N, dtype, "normal", seed=31)
@@ -215,7 +239,7 @@ def test_misaligned_input_pointer(dtype):
     xt = to_device(flat, dtype)
     out_idx = torch.empty((rows, k), dtype=torch.int32, device=DEV)
     out_val = torch.empty((rows, k), dtype=xt.dtype, device=DEV)
-    code = ds.DS_FP32 if dtype == "fp32" else ds.DS_BF16
+    code = {"fp32": ds.DS_FP32, "bf16": ds.DS_BF16, "fp16": ds.DS_FP16}[dtype]
     plan = ds.ds_topk_plan(xt.data_ptr() + esz, code, rows, N, k, 256, 256, 1)
     assert plan["async_copy"] == 0
     ds.ds_topk_ex(xt.data_ptr() + esz, code, rows, None, N, k, 256, 256, 7, 1,

@@ -19,6 +19,7 @@ DS_EUNSUPPORTED = -2
 DS_ECUDA = -3
 DS_FP32 = 0
 DS_BF16 = 1
+DS_FP16 = 2
 
 ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_plan", "ds_topk_max_k",
                 "ds_strerror", "ds_last_error_detail"]
@@ -150,12 +151,14 @@ def dtype_code(t):
         return DS_FP32
     if t.dtype == torch.bfloat16:
         return DS_BF16
-    raise TypeError("x must be float32 or bfloat16, got %s" % t.dtype)
+    if t.dtype == torch.float16:
+        return DS_FP16
+    raise TypeError("x must be float32, bfloat16 or float16, got %s" % t.dtype)
 
 
 def topk(x, k, B, B2, seed=0x5EED5EED, row_len=None, splits=0, stats=False, out_idx=None,
          out_val=None, stream=None):
-    """Top-k of every row of a 2-D CUDA tensor x (float32 or bfloat16).
+    """Top-k of every row of a 2-D CUDA tensor x (float32, bfloat16 or float16).
 
     Returns (idx int32 [rows, k], val [rows, k]) and, with stats=True, also an
     int64 [rows, splits, 4] tensor of (A, R, W, peak) per slice.

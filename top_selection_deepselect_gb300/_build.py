@@ -7,7 +7,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libds_topk.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("ds_topk.cu", "ds_kernels_fp32.cu", "ds_kernels_bf16.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("ds_topk.cu", "ds_kernels_fp32.cu", "ds_kernels_bf16.cu",
+                                         "ds_kernels_fp16.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ds_device.cuh"), os.path.join(CSRC, "ds_kernel.cuh"),
                   os.path.join(INCLUDE, "ds_topk.h")]
 

@@ -15,6 +15,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -94,6 +95,34 @@ struct Elem<1> {  // bf16
     __device__ static __forceinline__ uint32_t splat(uint32_t bits) { return bits | (bits << 16); }
 };
 
+template <>
+struct Elem<2> {  // IEEE binary16: +inf is 0x7C00, larger magnitudes are NaN
+    static constexpr int kSize = 2;
+    static constexpr int kPerChunk = 8;
+    static constexpr int kKeyTopShift = 40;
+    static constexpr int kKeyDigits = 2;
+    static constexpr uint32_t kNanKey = 0xFFFFu;
+    static constexpr uint32_t kInfKey = 0xFC00u;
+    static constexpr uint32_t kZeroKey = 0x8000u;
+    static constexpr uint32_t kNegInfBits = 0xFC00u;
+    static constexpr uint32_t kNanBits = 0x7E00u;
+    static constexpr uint32_t kThresholdInit = 0xFC00u;
+
+    __device__ static __forceinline__ uint32_t key(uint32_t u)
+    {
+        u &= 0xFFFFu;
+        uint32_t flipped = (u & 0x8000u) ? (~u & 0xFFFFu) : (u | 0x8000u);
+        uint32_t mag = u & 0x7FFFu;
+        flipped = (mag == 0u) ? kZeroKey : flipped;
+        return (mag > 0x7C00u) ? kNanKey : flipped;
+    }
+    __device__ static __forceinline__ uint32_t bits_of_key(uint32_t kk)
+    {
+        return (kk & 0x8000u) ? (kk ^ 0x8000u) : (~kk & 0xFFFFu);
+    }
+    __device__ static __forceinline__ uint32_t splat(uint32_t bits) { return bits | (bits << 16); }
+};
+
 // ---------------------------------------------------------------------------
 // Running threshold T of the scan ("算法": starts at -inf, raised to the
 // smallest kept element after every compaction), held as the composite of
@@ -110,7 +139,7 @@ struct Elem<1> {  // bf16
 struct Threshold {
     unsigned long long comp;  // composite of T; 0 admits every element
     uint32_t ti;              // index of T (elements with T's key pass iff index < ti)
-    uint32_t t_ge, t_gt;      // prefilter operands (fp32 bits or packed bf16x2)
+    uint32_t t_ge, t_gt;      // prefilter operands (fp32 bits or packed bf16x2 / f16x2)
     bool nan_ge, nan_gt;      // operand is NaN: the prefilter admits all, refine
 };
 

@@ -70,9 +70,20 @@ struct BlockView {
     bool plain;                 // no refinement and no partial chunk
 };
 
+// Packed unordered a >= t per 16-bit half (0xFFFF where it holds): bf16x2
+// for DT = 1, f16x2 for DT = 2.
+template <int DT>
+__device__ __forceinline__ uint32_t geu2_mask(uint32_t a, uint32_t t)
+{
+    if (DT == 1)
+        return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&a),
+                            *reinterpret_cast<const __nv_bfloat162 *>(&t));
+    return __hgeu2_mask(*reinterpret_cast<const __half2 *>(&a), *reinterpret_cast<const __half2 *>(&t));
+}
+
 // Prefilter bits of one 16-byte chunk, bit e = element e: !(v < t).
-// bf16: the packed unordered compare gives 0xFFFF per passing half; prmt
-// gathers one byte per element and dp4a folds four 0/1 bytes into four bits
+// bf16 / fp16: the packed unordered compare gives 0xFFFF per passing half;
+// prmt gathers one byte per element and dp4a folds four 0/1 bytes into four bits
 // (section "实现": set.bf16x2 / prmt / dp4a mask generation).
 template <int DT>
 __device__ __forceinline__ uint32_t prefilter_bits(const uint4 v, uint32_t t)
@@ -83,11 +94,10 @@ __device__ __forceinline__ uint32_t prefilter_bits(const uint4 v, uint32_t t)
                ((uint32_t)!(__uint_as_float(v.z) < tf) << 2) |
                ((uint32_t)!(__uint_as_float(v.w) < tf) << 3);
     } else {
-        const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-        const uint32_t m0 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.x), t2);
-        const uint32_t m1 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.y), t2);
-        const uint32_t m2 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.z), t2);
-        const uint32_t m3 = __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&v.w), t2);
+        const uint32_t m0 = geu2_mask<DT>(v.x, t);
+        const uint32_t m1 = geu2_mask<DT>(v.y, t);
+        const uint32_t m2 = geu2_mask<DT>(v.z, t);
+        const uint32_t m3 = geu2_mask<DT>(v.w, t);
         const uint32_t lo4 = __byte_perm(m0, m1, 0x7531) & 0x01010101u;
         const uint32_t hi4 = __byte_perm(m2, m3, 0x7531) & 0x01010101u;
         return (uint32_t)__dp4a(lo4, 0x08040201u, 0u) | ((uint32_t)__dp4a(hi4, 0x08040201u, 0u) << 4);
@@ -162,12 +172,24 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
     return r;
 }
 
+__device__ __forceinline__ uint32_t max_nan_f16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// NaN-propagating maximum of two packed (DT = 1, 2) or single (DT = 0) values.
+template <int DT>
+__device__ __forceinline__ uint32_t max_nan(uint32_t a, uint32_t b)
+{
+    return DT == 0 ? max_nan_f32(a, b) : DT == 1 ? max_nan_bf16x2(a, b) : max_nan_f16x2(a, b);
+}
+
 template <int DT>
 __device__ __forceinline__ uint32_t chunk_max(const uint4 v)
 {
-    if (DT == 0)
-        return max_nan_f32(max_nan_f32(v.x, v.y), max_nan_f32(v.z, v.w));
-    return max_nan_bf16x2(max_nan_bf16x2(v.x, v.y), max_nan_bf16x2(v.z, v.w));
+    return max_nan<DT>(max_nan<DT>(v.x, v.y), max_nan<DT>(v.z, v.w));
 }
 
 // true if some element summarised by the running maximum m passes !(x < t)
@@ -176,8 +198,7 @@ __device__ __forceinline__ bool max_passes(uint32_t m, uint32_t t)
 {
     if (DT == 0)
         return !(__uint_as_float(m) < __uint_as_float(t));
-    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162 *>(&t);
-    return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&m), t2) != 0u;
+    return geu2_mask<DT>(m, t) != 0u;
 }
 
 // Survivors of this warp's chunks.  Fast path: every lane folds its chunks
@@ -196,13 +217,12 @@ __device__ __forceinline__ int warp_filter(const BlockView &bv, const Threshold 
     for (int i = 0; i < M::kWords; ++i)
         mk.w[i] = 0u;
     // the identity of the maximum: -inf (any real element or NaN replaces it)
-    uint32_t mx = DT == 0 ? 0xFF800000u : 0xFF80FF80u;
+    uint32_t mx = Elem<DT>::splat(Elem<DT>::kNegInfBits);
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
         const int c = bv.c0 + lane + 32 * r;
         if (c < bv.c1)
-            mx = DT == 0 ? max_nan_f32(mx, chunk_max<DT>(lds128(bv.slot + c * 16)))
-                         : max_nan_bf16x2(mx, chunk_max<DT>(lds128(bv.slot + c * 16)));
+            mx = max_nan<DT>(mx, chunk_max<DT>(lds128(bv.slot + c * 16)));
     }
     const bool pass = bv.c0 + lane < bv.c1 && max_passes<DT>(mx, bv.t);
     if (!__any_sync(kFull, pass))
@@ -758,5 +778,6 @@ typedef void (*KernelFn)(Params);
 // Kernel entry points of one dtype, defined in ds_kernels_<dtype>.cu.
 KernelFn kernel_fp32(bool async, bool wide);
 KernelFn kernel_bf16(bool async, bool wide);
+KernelFn kernel_fp16(bool async, bool wide);
 
 }  // namespace ds

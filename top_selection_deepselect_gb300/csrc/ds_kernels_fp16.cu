@@ -1,0 +1,13 @@
+// ds_kernels_fp16.cu -- IEEE fp16 instantiations of the DeepSelect top-k kernel.
+#include "ds_kernel.cuh"
+
+namespace ds {
+
+KernelFn kernel_fp16(bool async, bool wide)
+{
+    if (async)
+        return wide ? deepselect_topk_kernel<2, true, 16> : deepselect_topk_kernel<2, true, 4>;
+    return wide ? deepselect_topk_kernel<2, false, 16> : deepselect_topk_kernel<2, false, 4>;
+}
+
+}  // namespace ds

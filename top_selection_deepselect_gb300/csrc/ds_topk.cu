@@ -1,7 +1,7 @@
 // ds_topk.cu -- host side of the DeepSelect top-k library: argument checks,
 // launch planning (split factor, ring depth, shared-memory layout) and the C
 // ABI declared in include/ds_topk.h.  The kernel itself is in ds_kernel.cuh,
-// instantiated per dtype in ds_kernels_fp32.cu and ds_kernels_bf16.cu.
+// instantiated per dtype in ds_kernels_fp32.cu, ds_kernels_bf16.cu and ds_kernels_fp16.cu.
 
 #include "ds_topk.h"
 
@@ -91,12 +91,13 @@ int device_info(DevInfo **out, int *dev_out)
 
 using ds::KernelFn;
 
-// 8 instantiations: dtype x asynchronous copies x mask rounds (4 rounds cover
+// 12 instantiations: dtype x asynchronous copies x mask rounds (4 rounds cover
 // blocks of up to 2 KiB per warp, 16 up to 8 KiB per warp).
 KernelFn kernel_for(int dtype, bool async, bool wide, int *slot)
 {
     *slot = dtype * 4 + (async ? 2 : 0) + (wide ? 1 : 0);
-    return dtype == DS_FP32 ? ds::kernel_fp32(async, wide) : ds::kernel_bf16(async, wide);
+    return dtype == DS_FP32 ? ds::kernel_fp32(async, wide)
+         : dtype == DS_BF16 ? ds::kernel_bf16(async, wide) : ds::kernel_fp16(async, wide);
 }
 
 int ensure_attributes(DevInfo &d, int dtype, bool async, bool wide, KernelFn *fn)
@@ -120,8 +121,8 @@ int ensure_attributes(DevInfo &d, int dtype, bool async, bool wide, KernelFn *fn
 int check_args(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits,
                const void *out_idx, const void *out_val)
 {
-    if (dtype != DS_FP32 && dtype != DS_BF16)
-        return fail(DS_EUNSUPPORTED, "dtype %d is not DS_FP32 (0) or DS_BF16 (1)", dtype);
+    if (dtype != DS_FP32 && dtype != DS_BF16 && dtype != DS_FP16)
+        return fail(DS_EUNSUPPORTED, "dtype %d is not DS_FP32 (0), DS_BF16 (1) or DS_FP16 (2)", dtype);
     if (rows < 0)
         return fail(DS_EINVAL, "rows = %d is negative", rows);
     if (N < 1 || N >= (int64_t)1 << 31)
@@ -499,8 +500,8 @@ int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, in
 int ds_topk_max_k(int dtype, int B, int B2)
 {
     g_detail[0] = '\0';
-    if (dtype != DS_FP32 && dtype != DS_BF16)
-        return fail(DS_EUNSUPPORTED, "dtype %d is not DS_FP32 or DS_BF16", dtype);
+    if (dtype != DS_FP32 && dtype != DS_BF16 && dtype != DS_FP16)
+        return fail(DS_EUNSUPPORTED, "dtype %d is not DS_FP32, DS_BF16 or DS_FP16", dtype);
     if (B < 1 || B2 < 1)
         return fail(DS_EINVAL, "B and B2 must be >= 1");
     DevInfo *d = nullptr;
