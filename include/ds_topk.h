@@ -120,6 +120,20 @@ int ds_topk_host(const void *x_host, int dtype, int rows, const int32_t *row_len
                  void *stream);
 
 /*
+ * ds_topk_host_async -- ds_topk_host without the final synchronisation: the
+ * copies and the selection are only enqueued on `stream`; the host buffers
+ * must stay valid and unmodified (inputs) or unread (outputs) until the
+ * stream reaches this point (cudaStreamSynchronize or an event).  With two
+ * streams and two sets of staging buffers, consecutive calls overlap one
+ * call's copies with the other's selection.  Page-locked host memory is
+ * needed for the copies to be asynchronous.
+ */
+int ds_topk_host_async(const void *x_host, int dtype, int rows, const int32_t *row_len_host,
+                       int64_t N, int k, int B, int B2, uint64_t seed, int32_t *out_idx_host,
+                       void *out_val_host, void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev,
+                       void *out_val_dev, void *stream);
+
+/*
  * ds_topk_plan -- the launch plan ds_topk_ex would use on the current device
  * (x is only inspected for its alignment).  splits as in ds_topk_ex.
  */

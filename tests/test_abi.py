@@ -98,6 +98,13 @@ def test_host_entry_checks_staging_buffers(lib):
     rc = lib.ds_topk_host(FAKE, ds.DS_FP32, 2, None, 64, 4, 16, 16, ctypes.c_uint64(0),
                           FAKE, FAKE, None, None, FAKE, FAKE, None)
     assert rc == ds.DS_EINVAL          # no device staging for x
+    for fn in (lib.ds_topk_host, lib.ds_topk_host_async):
+        rc = fn(FAKE, ds.DS_FP32, 2, FAKE, 64, 4, 16, 16, ctypes.c_uint64(0),
+                FAKE, FAKE, FAKE, None, FAKE, FAKE, None)
+        assert rc == ds.DS_EINVAL      # row_len_host given without row_len_dev
+        rc = fn(FAKE, ds.DS_FP32, 2, None, 64, 65, 16, 16, ctypes.c_uint64(0),
+                FAKE, FAKE, FAKE, None, FAKE, FAKE, None)
+        assert rc == ds.DS_EINVAL      # k > N
 
 
 def test_python_wrapper_raises_with_detail(lib):

@@ -309,6 +309,36 @@ def test_host_buffer_entry_point(name):
         assert_same(oi_host.numpy(), got_val, ref_idx, ref_val)
 
 
+@pytest.mark.parametrize("name", ["dsa_index_bf16", "small_fp32"])
+def test_host_async_entry_point_on_two_streams(name):
+    # consecutive enqueue-only calls on two streams with two staging sets,
+    # every result read back on the host after its stream completes
+    c, bits, row_len, (ref_idx, ref_val) = config_case(name)
+    rows, N, k = c["rows"], c["N"], c["k"]
+    tdt = torch.float32 if c["dtype"] == "fp32" else torch.bfloat16
+    x_host = torch.from_numpy(bits.view(np.int32 if c["dtype"] == "fp32" else np.int16)).pin_memory()
+    code = ds.DS_FP32 if c["dtype"] == "fp32" else ds.DS_BF16
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    sets = [dict(oi_host=torch.empty((rows, k), dtype=torch.int32).pin_memory(),
+                 ov_host=torch.empty((rows, k), dtype=x_host.dtype).pin_memory(),
+                 x_dev=torch.empty((rows, N), dtype=tdt, device=DEV),
+                 oi_dev=torch.empty((rows, k), dtype=torch.int32, device=DEV),
+                 ov_dev=torch.empty((rows, k), dtype=tdt, device=DEV)) for _ in range(2)]
+    for i in range(6):
+        b = sets[i % 2]
+        b["oi_host"].fill_(-7)
+        ds.ds_topk_host_async(x_host.data_ptr(), code, rows, None, N, k, c["B"], c["B2"], SEED + i,
+                              b["oi_host"].data_ptr(), b["ov_host"].data_ptr(), b["x_dev"].data_ptr(),
+                              None, b["oi_dev"].data_ptr(), b["ov_dev"].data_ptr(),
+                              streams[i % 2].cuda_stream)
+        if i > 0:
+            p = sets[(i - 1) % 2]
+            streams[(i - 1) % 2].synchronize()
+            got_val = p["ov_host"].numpy().view(np.uint32 if c["dtype"] == "fp32" else np.uint16)
+            assert_same(p["oi_host"].numpy(), got_val, ref_idx, ref_val)
+    torch.cuda.synchronize()
+
+
 def test_plans_of_the_workloads():
     for name in workloads.CONFIG_ORDER:
         c = workloads.CONFIGS[name]

@@ -21,8 +21,8 @@ DS_FP32 = 0
 DS_BF16 = 1
 DS_FP16 = 2
 
-ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_plan", "ds_topk_max_k",
-                "ds_strerror", "ds_last_error_detail"]
+ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_host_async", "ds_topk_plan",
+                "ds_topk_max_k", "ds_strerror", "ds_last_error_detail"]
 
 
 class DSError(RuntimeError):
@@ -69,6 +69,9 @@ def load_library(path=None):
         lib.ds_topk_host.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, vp, vp,
                                      vp, vp, vp, vp, vp]
         lib.ds_topk_host.restype = i32
+        lib.ds_topk_host_async.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, vp, vp,
+                                           vp, vp, vp, vp, vp]
+        lib.ds_topk_host_async.restype = i32
         lib.ds_topk_plan.argtypes = [vp, i32, i32, i64, i32, i32, i32, i32,
                                      ctypes.POINTER(ds_plan_t)]
         lib.ds_topk_plan.restype = i32
@@ -120,6 +123,14 @@ def ds_topk_host(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_h
                                                _u64(seed), out_idx_host, out_val_host, x_dev,
                                                row_len_dev, out_idx_dev, out_val_dev, stream),
                   "ds_topk_host")
+
+
+def ds_topk_host_async(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_host,
+                       out_val_host, x_dev, row_len_dev, out_idx_dev, out_val_dev, stream):
+    return _check(load_library().ds_topk_host_async(x_host, dtype, rows, row_len_host, N, k, B, B2,
+                                                     _u64(seed), out_idx_host, out_val_host, x_dev,
+                                                     row_len_dev, out_idx_dev, out_val_dev, stream),
+                  "ds_topk_host_async")
 
 
 def ds_topk_plan(x, dtype, rows, N, k, B, B2, splits=0):

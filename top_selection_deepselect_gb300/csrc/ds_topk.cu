@@ -426,10 +426,10 @@ int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64
                   (cudaStream_t)stream);
 }
 
-int ds_topk_host(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
-                 int k, int B, int B2, uint64_t seed, int32_t *out_idx_host, void *out_val_host,
-                 void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev, void *out_val_dev,
-                 void *stream)
+static int host_call(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
+                     int k, int B, int B2, uint64_t seed, int32_t *out_idx_host, void *out_val_host,
+                     void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev, void *out_val_dev,
+                     void *stream, bool sync)
 {
     g_detail[0] = '\0';
     int rc = check_args(x_host, dtype, rows, N, k, B, B2, 0, out_idx_host, out_val_host);
@@ -462,10 +462,30 @@ int ds_topk_host(const void *x_host, int dtype, int rows, const int32_t *row_len
     e = cudaMemcpyAsync(out_val_host, out_val_dev, (size_t)rows * k * es, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaMemcpyAsync(out_val)");
+    if (!sync)
+        return DS_OK;
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaStreamSynchronize");
     return DS_OK;
+}
+
+int ds_topk_host(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
+                 int k, int B, int B2, uint64_t seed, int32_t *out_idx_host, void *out_val_host,
+                 void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev, void *out_val_dev,
+                 void *stream)
+{
+    return host_call(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_host,
+                     out_val_host, x_dev, row_len_dev, out_idx_dev, out_val_dev, stream, true);
+}
+
+int ds_topk_host_async(const void *x_host, int dtype, int rows, const int32_t *row_len_host,
+                       int64_t N, int k, int B, int B2, uint64_t seed, int32_t *out_idx_host,
+                       void *out_val_host, void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev,
+                       void *out_val_dev, void *stream)
+{
+    return host_call(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_host,
+                     out_val_host, x_dev, row_len_dev, out_idx_dev, out_val_dev, stream, false);
 }
 
 int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits,
