@@ -13,7 +13,7 @@ its batch from DRAM.  The K timed launches are replayed from CUDA graphs and
 bracketed by CUDA events on the launching stream (plus a barrier and a
 device synchronize on both sides).  "e2e" times the host-buffer entry
 points: pinned host input -> device -> top-k -> pinned host output every
-step, two steps in flight on two streams (ds_topk_host_async), and also
+step, four steps in flight on four streams (ds_topk_host_async), and also
 synchronised every step (ds_topk_host).
 
 Multi-GPU (torchrun): every rank runs its own full batch (weak scaling, no
@@ -366,19 +366,22 @@ def time_e2e(torch, ds, wl, steps):
     return c["rows"] * steps / dt, h2d, d2h
 
 
-def time_e2e_pipelined(torch, ds, wl, steps):
-    """ds_topk_host_async on two streams with two staging sets: every step
-    copies its input from pinned host memory, selects and copies its result
-    back; after enqueuing step i the host waits for step i-1 and reads its
-    result, so one step's copies overlap the other's selection."""
+E2E_DEPTH = 4  # steps in flight in the end-to-end measurement
+
+
+def time_e2e_pipelined(torch, ds, wl, steps, depth=2):
+    """ds_topk_host_async on `depth` streams with as many staging sets: every
+    step copies its input from pinned host memory, selects and copies its
+    result back; after enqueuing step i the host waits for step i-depth+1 and
+    reads its result, so copies and selections of neighbouring steps overlap."""
     c = wl.c
     tdt = wl.x.dtype
     host_dtype = torch.int32 if c["dtype"] == "fp32" else torch.int16
     x_host = torch.from_numpy(wl.bits.view(np.int32 if c["dtype"] == "fp32" else np.int16)).pin_memory()
     rl_host = None if wl.row_len_np is None else torch.from_numpy(wl.row_len_np).pin_memory()
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in range(depth)]
     sets = []
-    for _ in range(2):
+    for _ in range(depth):
         sets.append(dict(
             oi_host=torch.empty((c["rows"], c["k"]), dtype=torch.int32).pin_memory(),
             ov_host=torch.empty((c["rows"], c["k"]), dtype=host_dtype).pin_memory(),
@@ -390,7 +393,7 @@ def time_e2e_pipelined(torch, ds, wl, steps):
     checksum = 0
 
     def issue(i):
-        st, b = streams[i % 2], sets[i % 2]
+        st, b = streams[i % depth], sets[i % depth]
         ds.ds_topk_host_async(x_host.data_ptr(), wl.code, c["rows"],
                               None if rl_host is None else rl_host.data_ptr(), c["N"], c["k"],
                               c["B"], c["B2"], SEED, b["oi_host"].data_ptr(), b["ov_host"].data_ptr(),
@@ -401,11 +404,13 @@ def time_e2e_pipelined(torch, ds, wl, steps):
         nonlocal checksum
         for i in range(n):
             issue(i)
-            if i > 0:
-                streams[(i - 1) % 2].synchronize()
-                checksum += int(sets[(i - 1) % 2]["oi_host"][0, 0])   # the host reads the result
-        streams[(n - 1) % 2].synchronize()
-        checksum += int(sets[(n - 1) % 2]["oi_host"][0, 0])
+            j = i - depth + 1
+            if j >= 0:
+                streams[j % depth].synchronize()
+                checksum += int(sets[j % depth]["oi_host"][0, 0])   # the host reads the result
+        for j in range(max(0, n - depth + 1), n):
+            streams[j % depth].synchronize()
+            checksum += int(sets[j % depth]["oi_host"][0, 0])
 
     run(4)
     t0 = time.perf_counter()
@@ -509,12 +514,13 @@ def run_ours(args, rank, world):
     if rank == 0:
         e2e_steps = args.e2e_steps or args.steps
         e2e_sync, h2d, d2h = time_e2e(torch, ds, wl, e2e_steps)
-        e2e_pipe = time_e2e_pipelined(torch, ds, wl, e2e_steps)
+        e2e_pipe = time_e2e_pipelined(torch, ds, wl, e2e_steps, depth=E2E_DEPTH)
         line["e2e"] = {"value": e2e_pipe * world, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                       "path": "ds_topk_host_async on two streams (pinned host buffers; each step "
-                               "copies its input, selects, copies its result back; the host reads "
-                               "every step's result)",
+                       "path": "ds_topk_host_async, %d steps in flight on %d streams (pinned host "
+                               "buffers; each step copies its input, selects, copies its result "
+                               "back; the host reads every step's result); kernels of different "
+                               "steps may run concurrently" % (E2E_DEPTH, E2E_DEPTH),
                        "sync_per_step_value": e2e_sync * world,
                        "sync_per_step_path": "ds_topk_host, synchronised every step"}
     if rank == 0 and world == 1 and not args.no_extras:
