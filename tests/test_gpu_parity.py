@@ -173,6 +173,20 @@ def test_split_rows_with_a_large_union(dtype, kind):
         assert_same(idx, val, ref_idx, ref_val)
 
 
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("kind", ["normal", "constant", "levels", "specials", "ascending"])
+def test_split_rows_pruned_by_the_largest_slice_threshold(dtype, kind):
+    # 6144 < splits * k <= 8192: slices send CTA 0 only entries at or above
+    # the largest slice k-th composite (ties across slices, short and empty
+    # slices included)
+    bits, _ = workloads.generate(5, 50000, dtype, kind, seed=37, fraction=0.2, value=-1.5)
+    row_len = np.array([50000, 0, 900, 7000, 49999], dtype=np.int32)
+    for k, B, B2, splits in [(900, 512, 512, 7), (1024, 1024, 512, 8), (1600, 256, 1024, 4)]:
+        ref_idx, ref_val = oracle.topk(bits, dtype, k, row_len=row_len)
+        idx, val = run(bits, dtype, k, B, B2, row_len=row_len, splits=splits)
+        assert_same(idx, val, ref_idx, ref_val)
+
+
 @pytest.mark.parametrize("kind,rows,N,k,B,B2", [("normal", 64, 32768, 512, 1024, 1024),
                                                 ("gumbel_spikes", 16, 128000, 50, 1024, 1024),
                                                 ("adversarial", 8, 65536, 1024, 1024, 1024)])

@@ -466,6 +466,7 @@ struct Misc {
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
     int fill;                            // select: slots handed out in the compaction
     int runlen[16];                      // CTA 0 of a cluster: length of each slice's sorted run
+    unsigned long long tslice[16];       // split rows: every slice's k-th composite (0: fewer than k)
     int pass;                            // select: digit passes so far (histogram rotation)
     unsigned long long tmin;             // select: smallest selected composite
 };

@@ -525,8 +525,9 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
 {
     const int tid = threadIdx.x;
     W += n;
+    unsigned long long tk = 0ull;  // this slice's k-th composite (0: fewer than k entries)
     if (n > o.k)
-        radix_select_topk(cand, n, o.k, whist, holes, ms);
+        tk = radix_select_topk(cand, n, o.k, whist, holes, ms);
     const int cnt = n < o.k ? n : o.k;
     if (stats != nullptr && tid == 0) {
         long long *s = stats + ((long long)row * S + slice) * 4;
@@ -560,15 +561,61 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
             merge_runs_and_write<DT>(reinterpret_cast<unsigned long long *>(ring), S, o, row, xrow, ms);
         return;
     }
-    // otherwise CTA 0 selects the top k of the union and orders it
-    cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
-    if (tid == 0)
-        ms->merge_off = atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), cnt);
-    __syncthreads();
-    unsigned long long *dst =
-        cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
-    for (int i = tid; i < cnt; i += kThreads)
-        dst[i] = cand[i];
+    // otherwise CTA 0 selects the top k of the union and orders it.  For a
+    // large union: the row's k-th composite is at least every slice's k-th
+    // (that slice alone holds k entries at or above it), so a slice sends
+    // CTA 0 only its entries at or above the largest slice threshold --
+    // exact, and often only k entries in all (sorted or heavily tied rows).
+    // Used when the union would not fit the register select (S*k > 6144).
+    const bool prune = (long long)S * o.k > 24LL * kThreads;
+    if (prune && tid < S)
+        *cluster.map_shared_rank(&ms->tslice[slice], tid) = tk;
+    cluster.sync();  // thresholds published; every CTA has finished streaming; CTA 0's ring is free
+    unsigned long long tmax = 0ull;
+    if (prune)
+        for (int s2 = 0; s2 < S; ++s2)
+            tmax = ms->tslice[s2] > tmax ? ms->tslice[s2] : tmax;
+    if (!prune) {
+        if (tid == 0)
+            ms->merge_off = atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), cnt);
+        __syncthreads();
+        unsigned long long *dst =
+            cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
+        for (int i = tid; i < cnt; i += kThreads)
+            dst[i] = cand[i];
+    } else {
+        // the kept entries of each warp's stripes, then one remote atomic per
+        // CTA for the slots in CTA 0, then the stores
+        const int lane = tid & 31, warp = tid >> 5;
+        uint32_t mine = 0u;
+        for (int i0 = warp * 32; i0 < cnt; i0 += kThreads) {
+            const int i = i0 + lane;
+            mine += (uint32_t)__popc(__ballot_sync(kFull, i < cnt && cand[i] >= tmax));
+        }
+        if (lane == 0)
+            ms->wsum[warp] = mine;
+        __syncthreads();
+        if (tid == 0) {
+            int tot = 0;
+            for (int w = 0; w < kWarps; ++w)
+                tot += (int)ms->wsum[w];
+            ms->merge_off = tot ? atomicAdd(cluster.map_shared_rank(&ms->merge_count, 0), tot) : 0;
+        }
+        __syncthreads();
+        int base = ms->merge_off;
+        for (int w = 0; w < warp; ++w)
+            base += (int)ms->wsum[w];
+        unsigned long long *dst = cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0);
+        for (int i0 = warp * 32; i0 < cnt; i0 += kThreads) {
+            const int i = i0 + lane;
+            const unsigned long long c = i < cnt ? cand[i] : 0ull;
+            const bool keep = i < cnt && c >= tmax;
+            const uint32_t b = __ballot_sync(kFull, keep);
+            if (keep)
+                dst[base + __popc(b & lanemask_lt(lane))] = c;
+            base += __popc(b);
+        }
+    }
     cluster.sync();
     if (slice != 0)
         return;
