@@ -323,6 +323,93 @@ __device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, cons
             emit<DT>(p, obase, ranks[j], vals[j], xrow);
 }
 
+// Largest k for which CTA 0 merges the slices' sorted runs (every thread
+// holds at most kMergeOut outputs of a merge round in registers).
+constexpr int kMergeOut = 16;
+constexpr int kMergeMaxK = kThreads * kMergeOut;
+// Below this many entries in the union, CTA 0 selects from the union
+// directly (registers hold it) instead of merging sorted runs.
+constexpr int kMergeMinUnion = 8192;
+
+// Outputs [t0, t1) (at most kMergeOut) of the descending merge of runs A[0, la)
+// and B[0, lb): a merge-path search finds how many of the first t0 come from
+// A, then the two runs are walked.  Distinct nonzero entries; 0 pads.
+__device__ __forceinline__ void merge_chunk(const unsigned long long *A, int la,
+                                            const unsigned long long *B, int lb, int t0, int t1,
+                                            unsigned long long (&out)[kMergeOut])
+{
+    int lo = t0 - lb > 0 ? t0 - lb : 0, hi = t0 < la ? t0 : la;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] > B[t0 - mid - 1])
+            lo = mid + 1;
+        else
+            hi = mid;
+    }
+    int i = lo, j = t0 - lo;
+#pragma unroll
+    for (int q = 0; q < kMergeOut; ++q) {
+        if (q < t1 - t0) {
+            const unsigned long long a = i < la ? A[i] : 0ull;
+            const unsigned long long b = j < lb ? B[j] : 0ull;
+            const bool ta = a > b;
+            out[q] = ta ? a : b;
+            i += ta ? 1 : 0;
+            j += ta ? 0 : 1;
+        }
+    }
+}
+
+
+// Sorts the cnt distinct nonzero entries arr[0, cnt) descending, 256 < cnt
+// <= 2048 (used above 1024, where it beats ranking across runs of 256 per
+// warp); arr holds pow2_ceil(cnt) entries (the pads are 0 and sort last).
+// Each warp sorts runs of 64 in registers (bitonic), then runs are merged
+// pairwise in rounds of doubling width: every thread produces its own
+// consecutive outputs of a merge (merge-path search, then a walk), holds
+// them in registers across a barrier and stores them in place.  With TO_OUT
+// the last round writes the first kout outputs to the row instead.
+template <int DT, bool TO_OUT>
+__device__ __forceinline__ void merge_sort_desc(unsigned long long *arr, int cnt, int kout,
+                                                const Out &p, long long obase,
+                                                const unsigned char *xrow)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = pow2_ceil(cnt);  // 512, 1024 or 2048
+    for (int i = cnt + tid; i < P; i += kThreads)
+        arr[i] = 0ull;
+    __syncthreads();
+    for (int r = warp; r < P / 64; r += kWarps) {
+        unsigned long long v[2] = {arr[64 * r + lane], arr[64 * r + 32 + lane]};
+        warp_bitonic_regs<2>(v, lane, true);
+        arr[64 * r + lane] = v[0];
+        arr[64 * r + 32 + lane] = v[1];
+    }
+    __syncthreads();
+    const int per = P / kThreads;  // outputs per thread: 2, 4 or 8
+    const int t0 = tid * per;
+    const int lim = cnt < kout ? cnt : kout;
+    for (int w = 64; w < P; w *= 2) {
+        const int pair = t0 / (2 * w), local = t0 % (2 * w);
+        const unsigned long long *A = arr + (size_t)pair * 2 * w;
+        unsigned long long out[kMergeOut];
+        merge_chunk(A, w, A + w, w, local, local + per, out);
+        if (TO_OUT && 2 * w == P) {
+#pragma unroll
+            for (int q = 0; q < kMergeOut; ++q)
+                if (q < per && t0 + q < lim)
+                    emit<DT>(p, obase, t0 + q, out[q], xrow);
+            return;
+        }
+        __syncthreads();  // every read of this round's runs is done
+#pragma unroll
+        for (int q = 0; q < kMergeOut; ++q)
+            if (q < per)
+                arr[t0 + q] = out[q];
+        __syncthreads();
+    }
+}
+
 template <int DT>
 __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt, const Out &p, int row,
                                                const unsigned char *xrow)
@@ -350,7 +437,7 @@ __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt,
     } else if (cnt <= 1024) {
         emit_runs<DT, 4>(arr, cnt, p, obase, xrow);
     } else if (cnt <= 2048) {
-        emit_runs<DT, 8>(arr, cnt, p, obase, xrow);
+        merge_sort_desc<DT, true>(arr, cnt, p.k, p, obase, xrow);
     } else {
         const int P = pow2_ceil(cnt);
         for (int i = cnt + threadIdx.x; i < P; i += kThreads)
@@ -402,50 +489,13 @@ static __device__ __noinline__ void sort_desc_inplace(unsigned long long *arr, i
     } else if (cnt <= 1024) {
         sort_runs_inplace<4>(arr, cnt);
     } else if (cnt <= 2048) {
-        sort_runs_inplace<8>(arr, cnt);
+        merge_sort_desc<0, false>(arr, cnt, 0, Out{nullptr, nullptr, 0}, 0, nullptr);
     } else {
         const int P = pow2_ceil(cnt);
         for (int i = cnt + threadIdx.x; i < P; i += kThreads)
             arr[i] = 0ull;
         __syncthreads();
         bitonic_sort_smem(arr, P, true);
-    }
-}
-
-// Largest k for which CTA 0 merges the slices' sorted runs (every thread
-// holds at most kMergeOut outputs of a merge round in registers).
-constexpr int kMergeOut = 16;
-constexpr int kMergeMaxK = kThreads * kMergeOut;
-// Below this many entries in the union, CTA 0 selects from the union
-// directly (registers hold it) instead of merging sorted runs.
-constexpr int kMergeMinUnion = 8192;
-
-// Outputs [t0, t1) (at most kMergeOut) of the descending merge of runs A[0, la)
-// and B[0, lb): a merge-path search finds how many of the first t0 come from
-// A, then the two runs are walked.  Distinct nonzero entries; 0 pads.
-__device__ __forceinline__ void merge_chunk(const unsigned long long *A, int la,
-                                            const unsigned long long *B, int lb, int t0, int t1,
-                                            unsigned long long (&out)[kMergeOut])
-{
-    int lo = t0 - lb > 0 ? t0 - lb : 0, hi = t0 < la ? t0 : la;
-    while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (A[mid] > B[t0 - mid - 1])
-            lo = mid + 1;
-        else
-            hi = mid;
-    }
-    int i = lo, j = t0 - lo;
-#pragma unroll
-    for (int q = 0; q < kMergeOut; ++q) {
-        if (q < t1 - t0) {
-            const unsigned long long a = i < la ? A[i] : 0ull;
-            const unsigned long long b = j < lb ? B[j] : 0ull;
-            const bool ta = a > b;
-            out[q] = ta ? a : b;
-            i += ta ? 1 : 0;
-            j += ta ? 0 : 1;
-        }
     }
 }
 
