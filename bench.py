@@ -71,10 +71,16 @@ def parse_args():
 # helpers
 # ---------------------------------------------------------------------------
 def kernel_source_hash():
+    """Hash of the kernel sources' code: comments and blank space are left
+    out, so a profile summary stays valid across comment-only edits."""
+    import re
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

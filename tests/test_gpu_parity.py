@@ -200,6 +200,20 @@ def test_fp16_workload_shapes(kind, rows, N, k, B, B2, splits):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("kind", ["normal", "levels", "specials"])
+def test_output_orderings_of_every_size(dtype, kind):
+    # k on both sides of every ordering strategy: counting ranks (<= 256),
+    # ranks across warp runs (<= 1024), merge-path sort (<= 2048), shared-
+    # memory bitonic (above), with one CTA per row and with splits
+    bits, _ = workloads.generate(4, 12000, dtype, kind, seed=41, fraction=0.1)
+    for k in [255, 256, 257, 512, 513, 1024, 1025, 1500, 2048, 2049, 3000]:
+        ref_idx, ref_val = oracle.topk(bits, dtype, k)
+        for splits in [1, 2]:
+            idx, val = run(bits, dtype, k, 1024, 1024, splits=splits)
+            assert_same(idx, val, ref_idx, ref_val)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 def test_negative_zero_and_nan_bits_are_returned_as_read(dtype):
     f = np.zeros((4, 3000), dtype=np.float32)
     f[:, ::2] = -0.0

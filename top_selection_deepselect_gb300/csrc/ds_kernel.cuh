@@ -14,19 +14,23 @@
 //     ahead of the filter by 16-byte asynchronous copies (cp.async): each
 //     lane copies exactly the chunks it will filter and waits only on its
 //     own copy groups, so the ring needs no barrier of its own;
-//   * a stage holds one B-block per `warps_per_block` warps; each warp filters
-//     its part with one unordered compare per element (fp32 FSETP, bf16 packed
-//     set.geu); only chunks that may hold a survivor get exact bit masks,
-//     which are walked with __ffs and placed by ballot rank (section "实现":
-//     one-pass mask + __ffs placement);
+//   * a stage holds one B-block per `warps_per_block` warps; each lane folds
+//     its chunks into one NaN-propagating maximum and compares it once with
+//     an unordered test (fp32, or packed bf16x2 / f16x2); only lanes whose
+//     maximum passes build exact bit masks (packed compare, prmt, dp4a),
+//     which are walked with __ffs (section "实现": one-pass mask + __ffs
+//     placement) at slots from a warp scan of lane counts;
 //   * the blocks of a stage are filtered in parallel against the same T; a
 //     stage is cut at the first block after which the buffer would reach
 //     k + B2, the buffer is compacted, and the rest of the stage is filtered
 //     again with the new T -- exactly the block-by-block semantics, so the
 //     counters A, R, W and the peak length equal the step-by-step model's;
 //   * split rows (section "实现", last paragraph): each CTA of the cluster
-//     selects the top k of its contiguous slice and stores it into CTA 0's
-//     shared memory (distributed shared memory), CTA 0 selects and orders.
+//     selects the top k of its contiguous slice; the lists meet in CTA 0's
+//     shared memory (distributed shared memory), which selects and orders
+//     the union -- pruned to the entries at or above the largest slice
+//     threshold when the union is large -- or, for the largest unions,
+//     merges the slices' sorted lists.
 #pragma once
 
 #include <cooperative_groups.h>
