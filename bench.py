@@ -28,6 +28,7 @@ import hashlib
 import json
 import math
 import os
+import platform
 import subprocess
 import sys
 import tempfile
@@ -225,6 +226,25 @@ def oracle_rows_per_s(name, seconds=None, steps=None, warmup=0, rows_per_step=4)
     return done * step_rows / dt, dt, done, step_rows
 
 
+SPEC_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (context beside the measured copy bandwidth)
+
+
+def host_cpu():
+    """Model name and logical core count of the host, for the CPU baseline lines."""
+    model = platform.processor() or platform.machine()
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    if key == "model name":
+                        break
+    except OSError:
+        pass
+    return {"model": model, "logical_cores": os.cpu_count()}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -239,7 +259,7 @@ def run_reference(args, rank, world):
         "dtype": c["dtype"], "data": "synthetic (seeded; stands in for DSA index scores)",
         "config": cfg_desc(c, name),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu()},
         "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -538,7 +558,8 @@ def run_ours(args, rank, world):
             us = 1e3 * ms2 / args.steps
             gbs = w2.read_bytes / (us * 1e-6) / 1e9
             per[name] = {"us_per_call": us, "rows_per_s": w2.rows / (us * 1e-6), "gbs": gbs,
-                         "frac_of_measured_hbm": gbs / peak, "l2_defeated": w2.l2_defeated,
+                         "frac_of_measured_hbm": gbs / peak, "frac_of_spec_hbm": gbs / SPEC_HBM_GBS,
+                         "l2_defeated": w2.l2_defeated,
                          "algorithmic_bytes": w2.read_bytes, "plan": w2.plan,
                          "torch_topk": time_torch_topk(torch, w2, args.steps)}
             if w2 is not wl:
@@ -548,7 +569,8 @@ def run_ours(args, rank, world):
         rate, dt, done, step_rows = oracle_rows_per_s(args.workload, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": "%d rows of %s in %.1f s (rows cycled), single thread"
-                                          % (done * step_rows, args.workload, dt)}
+                                          % (done * step_rows, args.workload, dt),
+                                "host": host_cpu()}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
