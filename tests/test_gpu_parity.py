@@ -291,6 +291,27 @@ def test_largest_k_that_fits():
     assert e.value.status == ds.DS_EUNSUPPORTED
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_one_long_row(dtype):
+    # 2^25 elements in one row: sixteen slices of one cluster
+    bits, _ = workloads.generate(1, 1 << 25, dtype, "gumbel_spikes", seed=43, spikes=64)
+    ref_idx, ref_val = oracle.topk(bits, dtype, 100)
+    idx, val = run(bits, dtype, 100, 4096, 4096)
+    assert_same(idx, val, ref_idx, ref_val)
+    # the block order of a slice holds at most 4096 blocks: a small B is refused
+    # with a message, not run wrong
+    with pytest.raises(ds.DSError):
+        run(bits, dtype, 100, 256, 256)
+
+
+def test_many_short_rows():
+    # thousands of rows: many waves of one-CTA-per-row launches
+    bits, row_len = workloads.generate(6000, 700, "bf16", "ragged_normal", seed=47, min_len=1)
+    ref_idx, ref_val = oracle.topk(bits, "bf16", 16, row_len=row_len)
+    idx, val = run(bits, "bf16", 16, 128, 128, row_len=row_len)
+    assert_same(idx, val, ref_idx, ref_val)
+
+
 def test_poisoned_tail_is_never_read():
     """Past row_len the input holds NaN, which would win every comparison."""
     bits, row_len = workloads.generate(16, 50000, "fp32", "ragged_normal", seed=8, min_len=1)
