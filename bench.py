@@ -346,6 +346,7 @@ def time_steps(torch, wl, steps, warmup, dist=None, burn_seconds=0.5):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("deepselect timed steps: %s" % wl.name)
     start.record(stream)
     for _ in range(full):
         g_full.replay()
@@ -354,6 +355,7 @@ def time_steps(torch, wl, steps, warmup, dist=None, burn_seconds=0.5):
     end.record(stream)
     end.synchronize()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
     if dist is not None:
         dist.barrier()
     ms = start.elapsed_time(end)

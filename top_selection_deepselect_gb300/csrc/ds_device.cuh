@@ -24,6 +24,17 @@ namespace ds {
 constexpr int kThreads = 256;             // threads per CTA
 constexpr int kWarps = kThreads / 32;     // warps per CTA
 constexpr int kMaxStages = 4;             // deepest shared-memory ring
+
+// Bounds-checked builds (-DDS_CHECKED, built by the tests): DS_GUARD(ms,
+// cond, bit) records `bit` in the word ms->check and yields false when a
+// computed shared-memory range is out of bounds, so the write is skipped
+// instead of corrupting memory (nothing traps).  In the product build it is
+// the constant true and its condition is not compiled.
+#ifdef DS_CHECKED
+#define DS_GUARD(ms, cond, bit) ::ds::ds_guard((cond), (bit), (ms)->check)
+#else
+#define DS_GUARD(ms, cond, bit) true
+#endif
 constexpr int kMaxSplits = 16;            // largest thread-block cluster used
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -465,6 +476,7 @@ struct Misc {
     int merge_count;                     // CTA 0 of a cluster: entries received
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
     int fill;                            // select: slots handed out in the compaction
+    unsigned int *check;                 // bounds-checked builds: violation bits (null otherwise)
     int runlen[16];                      // CTA 0 of a cluster: length of each slice's sorted run
     unsigned long long tslice[16];       // split rows: every slice's k-th composite (0: fewer than k)
     int pass;                            // select: digit passes so far (histogram rotation)
@@ -555,6 +567,26 @@ __device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, 
         ms->sel_above = excl + before;
         ms->sel_eq = through - before;
     }
+}
+
+#ifdef DS_CHECKED
+__device__ __forceinline__ bool ds_guard(bool ok, unsigned int bit, unsigned int *word)
+{
+    if (!ok && word != nullptr)
+        atomicOr(word, bit);
+    return ok;
+}
+#endif
+
+// Entries flagged in `bits` (bit j = register slot j) over the whole warp.
+template <int R>
+__device__ __forceinline__ int warp_count(uint32_t bits)
+{
+    int tot = 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j)
+        tot += __popc(__ballot_sync(kFull, (bits >> j) & 1u));
+    return tot;
 }
 
 // Slots for the entries flagged in `bits` (bit j = register slot j) of all
@@ -682,7 +714,8 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         if (eq <= 32u) {
             // gather the tied entries; warp 0 ranks them
             const int base = warp_reserve(live, &ms->group_count, lane);
-            warp_scatter<R>(live, hi, lo, ms->group + base, lane);
+            if (DS_GUARD(ms, base + warp_count<R>(live) <= 32, 4u))
+                warp_scatter<R>(live, hi, lo, ms->group + base, lane);
             __syncthreads();
             if (warp == 0) {
                 const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
@@ -714,7 +747,9 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
     } else {
         sel |= live;
     }
-    warp_scatter<R>(sel, hi, lo, cand + warp_reserve(sel, &ms->fill, lane), lane);
+    const int cbase = warp_reserve(sel, &ms->fill, lane);
+    if (DS_GUARD(ms, cbase + warp_count<R>(sel) <= n, 2u))
+        warp_scatter<R>(sel, hi, lo, cand + cbase, lane);
     if (!exact) {
         // the chosen digit's entries are taken whole: the smallest of them
         // is the k-th composite

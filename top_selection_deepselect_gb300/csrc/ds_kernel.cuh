@@ -51,6 +51,7 @@ struct Params {
     long long *stats;     // counters {A, R, W, peak} per (row, slice), or null
     long long N;
     int k, B, B2;
+    unsigned int *check;  // bounds-checked builds: violation bits (null otherwise)
     uint32_t seed_lo, seed_hi;
     int splits;          // CTAs per row
     int wpb;             // warps per B-block (a power of two)
@@ -606,8 +607,9 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
         cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
         unsigned long long *dst =
             cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + (size_t)slice * o.k;
-        for (int i = tid; i < cnt; i += kThreads)
-            dst[i] = cand[i];
+        if (DS_GUARD(ms, (long long)slice * o.k + cnt <= cand - reinterpret_cast<unsigned long long *>(ring), 8u))
+            for (int i = tid; i < cnt; i += kThreads)
+                dst[i] = cand[i];
         if (tid == 0)
             *cluster.map_shared_rank(&ms->runlen[slice], 0) = cnt;
         cluster.sync();
@@ -635,8 +637,9 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
         __syncthreads();
         unsigned long long *dst =
             cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + ms->merge_off;
-        for (int i = tid; i < cnt; i += kThreads)
-            dst[i] = cand[i];
+        if (DS_GUARD(ms, ms->merge_off + cnt <= cand - reinterpret_cast<unsigned long long *>(ring), 16u))
+            for (int i = tid; i < cnt; i += kThreads)
+                dst[i] = cand[i];
     } else {
         // the kept entries of each warp's stripes, then one remote atomic per
         // CTA for the slots in CTA 0, then the stores
@@ -660,6 +663,8 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
         for (int w = 0; w < warp; ++w)
             base += (int)ms->wsum[w];
         unsigned long long *dst = cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0);
+        const int mine_total = (int)mine;
+        if (DS_GUARD(ms, base + mine_total <= cand - reinterpret_cast<unsigned long long *>(ring), 32u))
         for (int i0 = warp * 32; i0 < cnt; i0 += kThreads) {
             const int i = i0 + lane;
             const unsigned long long c = i < cnt ? cand[i] : 0ull;
@@ -727,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
     if (tid == 0) {
         ms->merge_count = 0;
         ms->pass = 0;
+        ms->check = p.check;
     }
     __syncthreads();
     sort_asc_small(perm, msl, P);
@@ -848,7 +854,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
                 }
             }
             const int gend = trig >= 0 ? trig : bps - 1;
-            if (mine && g <= gend && cnt)
+            if (mine && g <= gend && cnt &&
+                DS_GUARD(ms, n + before_me + cnt <= ((p.off_perm - p.off_cand) >> 3), 1u))
                 warp_append<DT, MAXR>(bv, lane, mk, lane_cnt, cand, n + before_me);
             A += run - n;
             peak = run > peak ? run : peak;

@@ -334,6 +334,26 @@ int cluster_capacity(DevInfo &d, KernelFn fn, const Plan &pl, int *nclusters)
     return DS_OK;
 }
 
+#ifdef DS_CHECKED
+// Bounds-checked builds only (the tests build one): a device word that the
+// kernels' DS_GUARD checks OR their violation bits into.
+unsigned int *g_check = nullptr;
+
+int check_word(unsigned int **out)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_check == nullptr) {
+        cudaError_t e = cudaMalloc(&g_check, sizeof(unsigned int));
+        if (e == cudaSuccess)
+            e = cudaMemset(g_check, 0, sizeof(unsigned int));
+        if (e != cudaSuccess)
+            return fail_cuda(e, "bounds-check word");
+    }
+    *out = g_check;
+    return DS_OK;
+}
+#endif
+
 int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int k, int B,
            int B2, uint64_t seed, int splits_req, int32_t *out_idx, void *out_val, int64_t *stats,
            cudaStream_t stream)
@@ -380,6 +400,12 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     p.out_val = out_val;
     p.stats = reinterpret_cast<long long *>(stats);
     p.seed_lo = (uint32_t)seed;
+#ifdef DS_CHECKED
+    if ((rc = check_word(&p.check)) != DS_OK)
+        return rc;
+#else
+    p.check = nullptr;
+#endif
     p.seed_hi = (uint32_t)(seed >> 32);
 
     cudaLaunchConfig_t cfg;
@@ -545,6 +571,24 @@ int ds_topk_max_k(int dtype, int B, int B2)
         return fail(DS_EUNSUPPORTED, "no k fits shared memory for B=%d, B2=%d", B, B2);
     return lo;
 }
+
+#ifdef DS_CHECKED
+// Bounds-checked builds only: the violation bits so far (0: none); `reset`
+// clears them.  Synchronises the device.
+int ds_check_word(uint32_t *out, int reset)
+{
+    unsigned int *w = nullptr;
+    int rc = check_word(&w);
+    if (rc != DS_OK)
+        return rc;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(out, w, sizeof(unsigned int), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && reset)
+        e = cudaMemset(w, 0, sizeof(unsigned int));
+    return e == cudaSuccess ? DS_OK : fail_cuda(e, "bounds-check word");
+}
+#endif
 
 const char *ds_strerror(int status)
 {
