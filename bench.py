@@ -232,16 +232,22 @@ SPEC_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (context beside the measured copy 
 def host_cpu():
     """Model name and logical core count of the host, for the CPU baseline lines."""
     model = platform.processor() or platform.machine()
+    fields = {}
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
-                key = line.split(":")[0].strip().lower()
-                if key in ("model name", "cpu part", "hardware") and ":" in line:
-                    model = line.split(":", 1)[1].strip()
-                    if key == "model name":
-                        break
+                if ":" in line:
+                    key, val = line.split(":", 1)
+                    fields.setdefault(key.strip().lower(), val.strip())
     except OSError:
         pass
+    if "model name" in fields:
+        model = fields["model name"]
+    elif "cpu part" in fields:
+        # Arm: implementer and part numbers (0x41 / 0xd4f is Neoverse V2)
+        known = {("0x41", "0xd4f"): "Arm Neoverse V2"}
+        key = (fields.get("cpu implementer", ""), fields["cpu part"])
+        model = known.get(key, "Arm implementer %s part %s" % key)
     return {"model": model, "logical_cores": os.cpu_count()}
 
 
