@@ -415,9 +415,123 @@ __device__ __forceinline__ void merge_sort_desc(unsigned long long *arr, int cnt
     }
 }
 
+// Orders 256 < cnt <= 1024 distinct entries and writes them: entries are
+// bucketed by their top eight varying bits (histogram, a scan from the top
+// bucket down, scatter into bucket order) and each entry is then ranked only
+// against the members of its own bucket.  Returns false, having written
+// nothing, when a bucket holds more than kBucketMax entries (the caller then
+// ranks across warp runs).  `scratch` is 768 free words of shared memory.
+constexpr int kBucketMax = 128;
+
+template <int DT>
+__device__ __forceinline__ bool bucket_sort_write(unsigned long long *arr, int cnt, const Out &p,
+                                                  long long obase, const unsigned char *xrow,
+                                                  uint32_t *scratch, Misc *ms)
+{
+    constexpr int R = 4;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t hi[R], lo[R], dg[R], valid = 0u;
+    uint32_t oh = 0u, ol = 0u, ah = ~0u, al = ~0u;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int i = tid + kThreads * j;
+        hi[j] = 0u;
+        lo[j] = 0u;
+        if (i < cnt) {
+            const unsigned long long c = arr[i];
+            hi[j] = (uint32_t)(c >> 32);
+            lo[j] = (uint32_t)c;
+            valid |= 1u << j;
+            oh |= hi[j];
+            ol |= lo[j];
+            ah &= hi[j];
+            al &= lo[j];
+        }
+    }
+    oh = __reduce_or_sync(kFull, oh);
+    ol = __reduce_or_sync(kFull, ol);
+    ah = __reduce_and_sync(kFull, ah);
+    al = __reduce_and_sync(kFull, al);
+    if (lane == 0) {
+        ms->wor[warp] = ((unsigned long long)oh << 32) | ol;
+        ms->wand[warp] = ((unsigned long long)ah << 32) | al;
+    }
+    uint32_t *cntb = scratch, *offb = scratch + 256, *fillb = scratch + 512;
+    cntb[tid] = 0u;
+    fillb[tid] = 0u;
+    __syncthreads();  // also: every load of arr is done
+    unsigned long long vo = 0ull, va = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        vo |= ms->wor[w];
+        va &= ms->wand[w];
+    }
+    const unsigned long long vary = vo ^ va;
+    const int h = 63 - __clzll((long long)vary);  // cnt > 1 distinct entries: vary != 0
+    const int sh = h >= 7 ? h - 7 : 0;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        dg[j] = (sh >= 32 ? hi[j] >> (sh - 32) : __funnelshift_r(lo[j], hi[j], sh)) & 255u;
+        if ((valid >> j) & 1u)
+            atomicAdd(&cntb[dg[j]], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // offb[d] = entries in higher buckets; lane l owns buckets 8l .. 8l+7
+        const uint4 q0 = *reinterpret_cast<const uint4 *>(cntb + lane * 8);
+        const uint4 q1 = *reinterpret_cast<const uint4 *>(cntb + lane * 8 + 4);
+        const uint32_t c[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+        const uint32_t tot = ((c[0] + c[1]) + (c[2] + c[3])) + ((c[4] + c[5]) + (c[6] + c[7]));
+        uint32_t suf = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const uint32_t o = __shfl_down_sync(kFull, suf, d);
+            if (lane + d < 32)
+                suf += o;
+        }
+        uint32_t run = suf - tot;  // entries in the buckets of higher lanes
+        uint32_t mx = 0u;
+#pragma unroll
+        for (int t = 7; t >= 0; --t) {
+            offb[lane * 8 + t] = run;
+            run += c[t];
+            mx = c[t] > mx ? c[t] : mx;
+        }
+        mx = __reduce_max_sync(kFull, mx);
+        if (lane == 0)
+            ms->sel_eq = mx;
+    }
+    __syncthreads();
+    if (ms->sel_eq > (uint32_t)kBucketMax)
+        return false;  // uniform: every thread read the same word
+    int slot[R];
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        slot[j] = 0;
+        if ((valid >> j) & 1u) {
+            slot[j] = (int)offb[dg[j]] + (int)atomicAdd(&fillb[dg[j]], 1u);
+            arr[slot[j]] = ((unsigned long long)hi[j] << 32) | lo[j];
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if ((valid >> j) & 1u) {
+            const unsigned long long e = ((unsigned long long)hi[j] << 32) | lo[j];
+            const int b0 = (int)offb[dg[j]], bn = (int)cntb[dg[j]];
+            int r = 0;
+            for (int i = b0; i < b0 + bn; ++i)
+                r += arr[i] > e ? 1 : 0;
+            if (b0 + r < p.k)
+                emit<DT>(p, obase, b0 + r, e, xrow);
+        }
+    }
+    return true;
+}
+
 template <int DT>
 __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt, const Out &p, int row,
-                                               const unsigned char *xrow)
+                                               const unsigned char *xrow, uint32_t *scratch, Misc *ms)
 {
     using E = Elem<DT>;
     const long long obase = (long long)row * p.k;
@@ -437,10 +551,13 @@ __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt,
                 rank += arr[j] > e ? 1 : 0;
             emit<DT>(p, obase, rank, e, xrow);
         }
-    } else if (cnt <= 512) {
-        emit_runs<DT, 2>(arr, cnt, p, obase, xrow);
     } else if (cnt <= 1024) {
-        emit_runs<DT, 4>(arr, cnt, p, obase, xrow);
+        if (!bucket_sort_write<DT>(arr, cnt, p, obase, xrow, scratch, ms)) {
+            if (cnt <= 512)
+                emit_runs<DT, 2>(arr, cnt, p, obase, xrow);
+            else
+                emit_runs<DT, 4>(arr, cnt, p, obase, xrow);
+        }
     } else if (cnt <= 2048) {
         merge_sort_desc<DT, true>(arr, cnt, p.k, p, obase, xrow);
     } else {
@@ -593,7 +710,7 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
     }
 
     if (S == 1) {
-        sort_and_write<DT>(cand, cnt, o, row, xrow);
+        sort_and_write<DT>(cand, cnt, o, row, xrow, whist, ms);
         return;
     }
 
@@ -683,7 +800,7 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
     unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
     if (total > kk)
         radix_select_topk(merged, total, kk, whist, holes, ms);
-    sort_and_write<DT>(merged, kk, o, row, xrow);
+    sort_and_write<DT>(merged, kk, o, row, xrow, whist, ms);
 }
 
 // ---------------------------------------------------------------------------
