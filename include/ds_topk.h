@@ -40,6 +40,7 @@
 #ifndef DS_TOPK_H
 #define DS_TOPK_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -132,6 +133,42 @@ int ds_topk_host_async(const void *x_host, int dtype, int rows, const int32_t *r
                        int64_t N, int k, int B, int B2, uint64_t seed, int32_t *out_idx_host,
                        void *out_val_host, void *x_dev, int32_t *row_len_dev, int32_t *out_idx_dev,
                        void *out_val_dev, void *stream);
+
+/*
+ * ds_topk_long_row -- top-k of ONE row of N elements spread over the whole
+ * GPU, sorted by (value desc, index asc), the same result as ds_topk with
+ * rows = 1.  The row is cut into G pieces of P elements (P a multiple of B;
+ * the last piece shorter), every piece is selected by its own CTA(s)
+ * (DeepSelect-deep-dive, section "实现", last paragraph: a sequence is cut
+ * into parts that are selected separately), the top k of the G*k piece
+ * results is selected by a second launch, and a gather maps the chosen
+ * positions back to row indices (the multi-pass selection of one long row in
+ * "CUDA 算子笔记 4", section "Top K Selection", takes the same place).  G
+ * grows with N / k up to two pieces per SM; when it would be 1 the row is
+ * selected directly and no workspace is used.
+ *   x          device, N elements of `dtype`
+ *   N, k, B, B2, seed  as in ds_topk (rows = 1)
+ *   workspace  caller-owned device memory, 256-byte aligned, of at least the
+ *              size ds_topk_long_row_workspace returns (may be NULL when that
+ *              size is 0); it holds the piece results between the launches
+ *              and must not be used by another call until this one is done
+ *              on `stream`
+ *   out_idx    device int32[k], row indices
+ *   out_val    device [k] elements of `dtype`
+ *   stream     cudaStream_t or NULL; three kernels are enqueued, nothing is
+ *              synchronised
+ * Errors: the argument checks of ds_topk, and DS_EINVAL when the workspace is
+ * NULL, misaligned or smaller than needed.
+ */
+int ds_topk_long_row(const void *x, int dtype, int64_t N, int k, int B, int B2, uint64_t seed,
+                     void *workspace, size_t workspace_bytes, int32_t *out_idx, void *out_val,
+                     void *stream);
+
+/* Plan of ds_topk_long_row for these arguments on the current device:
+ * *bytes = workspace bytes it needs (0: none); when non-NULL, *piece_len = P
+ * and *pieces = G (G = 1: the row is selected directly, P = N). */
+int ds_topk_long_row_workspace(int dtype, int64_t N, int k, int B, int B2, size_t *bytes,
+                               int64_t *piece_len, int *pieces);
 
 /*
  * ds_topk_plan -- the launch plan ds_topk_ex would use on the current device

@@ -126,3 +126,36 @@ def test_no_cuda_device_is_a_cuda_error(lib):
     rc = lib.ds_topk(FAKE, ds.DS_FP32, 1, None, 1024, 8, 128, 128, ctypes.c_uint64(0), FAKE,
                      FAKE, None)
     assert rc == ds.DS_ECUDA
+
+
+@pytest.mark.parametrize("args,status", [
+    (dict(dtype=3), ds.DS_EUNSUPPORTED),
+    (dict(N=0), ds.DS_EINVAL),
+    (dict(N=1 << 31), ds.DS_EINVAL),
+    (dict(k=0), ds.DS_EINVAL),
+    (dict(k=2049, N=2048), ds.DS_EINVAL),
+    (dict(B=0), ds.DS_EINVAL),
+    (dict(B2=0), ds.DS_EINVAL),
+    (dict(x=None), ds.DS_EINVAL),
+    (dict(out_idx=None), ds.DS_EINVAL),
+    (dict(out_val=None), ds.DS_EINVAL),
+])
+def test_long_row_argument_errors(lib, args, status):
+    a = dict(x=FAKE, dtype=ds.DS_FP32, N=1 << 24, k=64, B=1024, B2=1024, out_idx=FAKE,
+             out_val=FAKE)
+    a.update(args)
+    rc = lib.ds_topk_long_row(a["x"], a["dtype"], a["N"], a["k"], a["B"], a["B2"],
+                              ctypes.c_uint64(0), FAKE, 1 << 20, a["out_idx"], a["out_val"], None)
+    assert rc == status
+    assert ds.ds_last_error_detail()
+    if a["x"] and a["out_idx"] and a["out_val"]:
+        # the workspace query makes the same argument checks (it has no pointers)
+        n = ctypes.c_size_t(0)
+        rc = lib.ds_topk_long_row_workspace(a["dtype"], a["N"], a["k"], a["B"], a["B2"],
+                                            ctypes.byref(n), None, None)
+        assert rc == status
+
+
+def test_long_row_workspace_query_needs_an_output(lib):
+    assert lib.ds_topk_long_row_workspace(ds.DS_FP32, 1 << 24, 64, 1024, 1024, None, None,
+                                          None) == ds.DS_EINVAL

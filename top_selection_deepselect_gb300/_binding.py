@@ -21,8 +21,9 @@ DS_FP32 = 0
 DS_BF16 = 1
 DS_FP16 = 2
 
-ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_host_async", "ds_topk_plan",
-                "ds_topk_max_k", "ds_strerror", "ds_last_error_detail"]
+ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_host_async", "ds_topk_long_row",
+                "ds_topk_long_row_workspace", "ds_topk_plan", "ds_topk_max_k", "ds_strerror",
+                "ds_last_error_detail"]
 
 
 class DSError(RuntimeError):
@@ -72,6 +73,14 @@ def load_library(path=None):
         lib.ds_topk_host_async.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, vp, vp,
                                            vp, vp, vp, vp, vp]
         lib.ds_topk_host_async.restype = i32
+        lib.ds_topk_long_row.argtypes = [vp, i32, i64, i32, i32, i32, u64, vp, ctypes.c_size_t,
+                                         vp, vp, vp]
+        lib.ds_topk_long_row.restype = i32
+        lib.ds_topk_long_row_workspace.argtypes = [i32, i64, i32, i32, i32,
+                                                   ctypes.POINTER(ctypes.c_size_t),
+                                                   ctypes.POINTER(ctypes.c_int64),
+                                                   ctypes.POINTER(ctypes.c_int)]
+        lib.ds_topk_long_row_workspace.restype = i32
         lib.ds_topk_plan.argtypes = [vp, i32, i32, i64, i32, i32, i32, i32,
                                      ctypes.POINTER(ds_plan_t)]
         lib.ds_topk_plan.restype = i32
@@ -131,6 +140,22 @@ def ds_topk_host_async(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out
                                                      _u64(seed), out_idx_host, out_val_host, x_dev,
                                                      row_len_dev, out_idx_dev, out_val_dev, stream),
                   "ds_topk_host_async")
+
+
+def ds_topk_long_row(x, dtype, N, k, B, B2, seed, workspace, workspace_bytes, out_idx, out_val,
+                     stream):
+    return _check(load_library().ds_topk_long_row(x, dtype, N, k, B, B2, _u64(seed), workspace,
+                                                   workspace_bytes, out_idx, out_val, stream),
+                  "ds_topk_long_row")
+
+
+def ds_topk_long_row_workspace(dtype, N, k, B, B2, plan=False):
+    """Workspace bytes; with plan=True, (bytes, piece length P, pieces G)."""
+    n, P, G = ctypes.c_size_t(0), ctypes.c_int64(0), ctypes.c_int(0)
+    _check(load_library().ds_topk_long_row_workspace(dtype, N, k, B, B2, ctypes.byref(n),
+                                                     ctypes.byref(P), ctypes.byref(G)),
+           "ds_topk_long_row_workspace")
+    return (n.value, P.value, G.value) if plan else n.value
 
 
 def ds_topk_plan(x, dtype, rows, N, k, B, B2, splits=0):
@@ -202,4 +227,33 @@ def topk(x, k, B, B2, seed=0x5EED5EED, row_len=None, splits=0, stats=False, out_
                None if st_t is None else st_t.data_ptr(), stream.cuda_stream)
     if stats:
         return out_idx, out_val, st_t
+    return out_idx, out_val
+
+
+def topk_long_row(x, k, B, B2, seed=0x5EED5EED, workspace=None, out_idx=None, out_val=None,
+                  stream=None):
+    """Top-k of one long 1-D CUDA tensor x spread over the whole GPU.
+
+    Returns (idx int32 [k], val [k]).  The workspace (a CUDA uint8 tensor of
+    at least ds_topk_long_row_workspace bytes) is allocated with torch when not
+    given.
+    """
+    import torch
+    if x.dim() != 1 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 1-D CUDA tensor")
+    N = x.numel()
+    code = dtype_code(x)
+    need = ds_topk_long_row_workspace(code, N, k, B, B2)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    elif workspace.numel() < need:
+        raise ValueError("workspace has %d bytes, %d needed" % (workspace.numel(), need))
+    if out_idx is None:
+        out_idx = torch.empty(k, dtype=torch.int32, device=x.device)
+    if out_val is None:
+        out_val = torch.empty(k, dtype=x.dtype, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    ds_topk_long_row(x.data_ptr(), code, N, k, B, B2, seed, workspace.data_ptr(),
+                     workspace.numel(), out_idx.data_ptr(), out_val.data_ptr(), stream.cuda_stream)
     return out_idx, out_val

@@ -50,6 +50,7 @@ struct Params {
     void *out_val;
     long long *stats;     // counters {A, R, W, peak} per (row, slice), or null
     long long N;
+    long long total;      // elements in x: without row_len, row r holds min(N, total - r*N)
     int k, B, B2;
     unsigned int *check;  // bounds-checked builds: violation bits (null otherwise)
     uint32_t seed_lo, seed_hi;
@@ -822,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
     uint16_t *holes = reinterpret_cast<uint16_t *>(smem + p.off_holes);
     Misc *ms = reinterpret_cast<Misc *>(smem + p.off_misc);
 
-    long long len_ll = p.row_len ? (long long)p.row_len[row] : p.N;
+    long long len_ll = p.row_len ? (long long)p.row_len[row] : p.total - (long long)row * p.N;
     len_ll = len_ll < 0 ? 0 : (len_ll > p.N ? p.N : len_ll);
     const int len = (int)len_ll;
     const int B = p.B;

@@ -147,7 +147,6 @@ struct Plan {
 };
 
 
-// Shared-memory layout for a given split factor and ring depth.
 // Shared-memory layout for a given split factor and ring depth.  Every region
 // starts on a 128-byte boundary (asynchronous-copy destinations need 16 bytes, the
 // scratch words are read with 128-bit loads).
@@ -354,9 +353,11 @@ int check_word(unsigned int **out)
 }
 #endif
 
-int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int k, int B,
-           int B2, uint64_t seed, int splits_req, int32_t *out_idx, void *out_val, int64_t *stats,
-           cudaStream_t stream)
+// `total` = elements in x when row_len is NULL (rows * N for a matrix; less
+// when the rows are consecutive pieces of one long row with a short last piece).
+int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int64_t total,
+           int k, int B, int B2, uint64_t seed, int splits_req, int32_t *out_idx, void *out_val,
+           int64_t *stats, cudaStream_t stream)
 {
     int rc = check_args(x, dtype, rows, N, k, B, B2, splits_req, out_idx, out_val);
     if (rc != DS_OK)
@@ -396,6 +397,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     Params &p = pl.p;
     p.x = x;
     p.row_len = row_len;
+    p.total = total;
     p.out_idx = out_idx;
     p.out_val = out_val;
     p.stats = reinterpret_cast<long long *>(stats);
@@ -431,6 +433,128 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
 
 size_t elem_size(int dtype) { return dtype == DS_FP32 ? 4 : 2; }
 
+// ---------------------------------------------------------------------------
+// One long row over the whole GPU.  The row is cut into G pieces of P
+// elements (the last one shorter), viewed as a [G x P] matrix: the first
+// launch takes the exact top k of every piece, the second the top k of the
+// G*k piece results laid end to end, and a gather maps each chosen position
+// q back to the row index (q / k) * P + (index within piece q / k).
+//
+// Why the second launch's order is the row's order: a piece's results are
+// sorted by (value desc, index asc), pieces are laid out in row order, so
+// among equal values a smaller position means a smaller row index.  A last
+// piece shorter than k is padded with -inf at its end; with k <= N there are
+// at least k real entries, all ranked ahead of every pad (a pad ties only
+// with real -inf values and sits after all of them), so no pad is chosen.
+// ---------------------------------------------------------------------------
+constexpr long long kRowPieceMin = 64;  // pieces hold at least this many k
+constexpr size_t kWsAlign = 256;
+
+size_t align_ws(size_t v) { return (v + kWsAlign - 1) / kWsAlign * kWsAlign; }
+
+struct RowPlan {
+    long long P;        // piece length (a multiple of B and of 8 elements)
+    int G;              // pieces (1: the row is selected directly)
+    long long N2;       // row pitch of the second launch (G*k rounded up to 8)
+    size_t off_val1, off_q2, bytes;  // workspace layout; idx1 at offset 0
+};
+
+long long gcd_ll(long long a, long long b)
+{
+    while (b) {
+        const long long t = a % b;
+        a = b;
+        b = t;
+    }
+    return a;
+}
+
+int row_plan(int dtype, int64_t N, int k, int B, int sms, RowPlan &rp)
+{
+    memset(&rp, 0, sizeof(rp));
+    const long long unit = (long long)B / gcd_ll(B, 8) * 8;  // lcm(B, 8)
+    long long g = (long long)N / (kRowPieceMin * k);
+    if (g > 2LL * sms)
+        g = 2LL * sms;
+    if (g >= 8)
+        g = g / 8 * 8;
+    if (g < 2) {
+        rp.G = 1;
+        rp.P = N;
+        return DS_OK;
+    }
+    long long P = ((N + g - 1) / g + unit - 1) / unit * unit;
+    const long long Pmax = kMaxPermBlocks * B / unit * unit;  // the block order of one CTA
+    P = P < Pmax ? P : Pmax;
+    const long long Pk = ((long long)k + unit - 1) / unit * unit;
+    P = P > Pk ? P : Pk;
+    const long long G = (N + P - 1) / P;
+    if (G < 2) {
+        rp.G = 1;
+        rp.P = N;
+        return DS_OK;
+    }
+    rp.P = P;
+    rp.G = (int)G;
+    rp.N2 = (G * k + 7) / 8 * 8;
+    if (rp.N2 >= (long long)1 << 31)
+        return fail(DS_EUNSUPPORTED, "pieces * k = %lld exceeds 2^31", G * k);
+    const size_t es = elem_size(dtype);
+    rp.off_val1 = align_ws((size_t)G * k * 4);
+    rp.off_q2 = rp.off_val1 + align_ws((size_t)rp.N2 * es);
+    rp.bytes = rp.off_q2 + align_ws((size_t)k * 4);
+    return DS_OK;
+}
+
+__global__ void long_row_gather(const int32_t *__restrict__ q2, const int32_t *__restrict__ idx1,
+                                int k, long long P, int32_t *__restrict__ out_idx)
+{
+    const int j = blockIdx.x * blockDim.x + threadIdx.x;
+    if (j < k) {
+        const int q = q2[j];
+        const int li = q >= 0 ? idx1[q] : -1;
+        out_idx[j] = li >= 0 ? (int32_t)((long long)(q / k) * P + li) : -1;
+    }
+}
+
+int long_row_check(const void *x, int dtype, int64_t N, int k, int B, int B2, const void *out_idx,
+                   const void *out_val)
+{
+    return check_args(x, dtype, 1, N, k, B, B2, 0, out_idx, out_val);
+}
+
+int long_row_plan(int dtype, int64_t N, int k, int B, RowPlan &rp)
+{
+    DevInfo *d = nullptr;
+    int rc = device_info(&d, nullptr);
+    if (rc != DS_OK)
+        return rc;
+    return row_plan(dtype, N, k, B, d->sms, rp);
+}
+
+int long_row_run(const void *x, int dtype, int64_t N, int k, int B, int B2, uint64_t seed,
+                 const RowPlan &rp, unsigned char *ws, int32_t *out_idx, void *out_val,
+                 cudaStream_t stream)
+{
+    if (rp.G == 1)
+        return launch(x, dtype, 1, nullptr, N, N, k, B, B2, seed, 0, out_idx, out_val, nullptr,
+                      stream);
+    int32_t *idx1 = reinterpret_cast<int32_t *>(ws);
+    void *val1 = ws + rp.off_val1;
+    int32_t *q2 = reinterpret_cast<int32_t *>(ws + rp.off_q2);
+    int rc = launch(x, dtype, rp.G, nullptr, rp.P, N, k, B, B2, seed, 0, idx1, val1, nullptr,
+                    stream);
+    if (rc != DS_OK)
+        return rc;
+    rc = launch(val1, dtype, 1, nullptr, rp.N2, (int64_t)rp.G * k, k, B, B2, seed, 0, q2, out_val,
+                nullptr, stream);
+    if (rc != DS_OK)
+        return rc;
+    long_row_gather<<<(k + 255) / 256, 256, 0, stream>>>(q2, idx1, k, rp.P, out_idx);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DS_OK : fail_cuda(e, "long_row_gather launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -439,8 +563,8 @@ int ds_topk(const void *x, int dtype, int rows, const int32_t *row_len, int64_t 
             int B2, uint64_t seed, int32_t *out_idx, void *out_val, void *stream)
 {
     g_detail[0] = '\0';
-    return launch(x, dtype, rows, row_len, N, k, B, B2, seed, 0, out_idx, out_val, nullptr,
-                  (cudaStream_t)stream);
+    return launch(x, dtype, rows, row_len, N, (int64_t)rows * N, k, B, B2, seed, 0, out_idx, out_val,
+                  nullptr, (cudaStream_t)stream);
 }
 
 int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int k,
@@ -448,8 +572,8 @@ int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64
                int64_t *stats, void *stream)
 {
     g_detail[0] = '\0';
-    return launch(x, dtype, rows, row_len, N, k, B, B2, seed, splits, out_idx, out_val, stats,
-                  (cudaStream_t)stream);
+    return launch(x, dtype, rows, row_len, N, (int64_t)rows * N, k, B, B2, seed, splits, out_idx,
+                  out_val, stats, (cudaStream_t)stream);
 }
 
 static int host_call(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
@@ -478,8 +602,8 @@ static int host_call(const void *x_host, int dtype, int rows, const int32_t *row
         if (e != cudaSuccess)
             return fail_cuda(e, "cudaMemcpyAsync(row_len)");
     }
-    rc = launch(x_dev, dtype, rows, row_len_dev, N, k, B, B2, seed, 0, out_idx_dev, out_val_dev,
-                nullptr, s);
+    rc = launch(x_dev, dtype, rows, row_len_dev, N, (int64_t)rows * N, k, B, B2, seed, 0,
+                out_idx_dev, out_val_dev, nullptr, s);
     if (rc != DS_OK)
         return rc;
     e = cudaMemcpyAsync(out_idx_host, out_idx_dev, (size_t)rows * k * 4, cudaMemcpyDeviceToHost, s);
@@ -512,6 +636,47 @@ int ds_topk_host_async(const void *x_host, int dtype, int rows, const int32_t *r
 {
     return host_call(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_host,
                      out_val_host, x_dev, row_len_dev, out_idx_dev, out_val_dev, stream, false);
+}
+
+int ds_topk_long_row_workspace(int dtype, int64_t N, int k, int B, int B2, size_t *bytes,
+                               int64_t *piece_len, int *pieces)
+{
+    g_detail[0] = '\0';
+    if (!bytes)
+        return fail(DS_EINVAL, "bytes must be non-NULL");
+    int rc = long_row_check((const void *)16, dtype, N, k, B, B2, (const void *)16,
+                            (const void *)16);
+    if (rc != DS_OK)
+        return rc;
+    RowPlan rp;
+    if ((rc = long_row_plan(dtype, N, k, B, rp)) != DS_OK)
+        return rc;
+    *bytes = rp.bytes;
+    if (piece_len)
+        *piece_len = rp.P;
+    if (pieces)
+        *pieces = rp.G;
+    return DS_OK;
+}
+
+int ds_topk_long_row(const void *x, int dtype, int64_t N, int k, int B, int B2, uint64_t seed,
+                     void *workspace, size_t workspace_bytes, int32_t *out_idx, void *out_val,
+                     void *stream)
+{
+    g_detail[0] = '\0';
+    int rc = long_row_check(x, dtype, N, k, B, B2, out_idx, out_val);
+    if (rc != DS_OK)
+        return rc;
+    RowPlan rp;
+    if ((rc = long_row_plan(dtype, N, k, B, rp)) != DS_OK)
+        return rc;
+    if (rp.bytes > 0 && (!workspace || workspace_bytes < rp.bytes))
+        return fail(DS_EINVAL, "workspace of %zu bytes at %p is smaller than the %zu bytes needed; "
+                    "query ds_topk_long_row_workspace", workspace_bytes, workspace, rp.bytes);
+    if (rp.bytes > 0 && (uintptr_t)workspace % kWsAlign != 0)
+        return fail(DS_EINVAL, "workspace must be %zu-byte aligned", kWsAlign);
+    return long_row_run(x, dtype, N, k, B, B2, seed, rp, static_cast<unsigned char *>(workspace),
+                        out_idx, out_val, (cudaStream_t)stream);
 }
 
 int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits,

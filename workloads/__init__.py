@@ -46,6 +46,11 @@ CONFIGS = {
 CONFIG_ORDER = ["small_fp32", "dsa_index_bf16", "dsa_decode_ragged_fp32",
                 "sampling_logits_bf16", "adversarial_fp32"]
 
+# one row over the whole GPU (ds_topk_long_row): the single huge row of the
+# multi-pass selection in "CUDA 算子笔记 4", section "Top K Selection"
+LONG_ROW = dict(rows=1, N=1 << 27, dtype=FP32, k=1024, B=1024, B2=1024, kind="normal", seed=1006,
+                desc="one long row: 1 x 2^27 fp32 N(0,1), k=1024, B=B2=1024")
+
 
 def to_bf16_bits(f32):
     """Round float32 values to bfloat16 (nearest even) and return the uint16 bits."""
