@@ -171,6 +171,29 @@ int ds_topk_long_row_workspace(int dtype, int64_t N, int k, int B, int B2, size_
                                int64_t *piece_len, int *pieces);
 
 /*
+ * ds_topk_long_row_noalloc -- ds_topk_long_row for callers that cannot
+ * allocate device memory: the same operation, arguments and result, with the
+ * piece results kept in a workspace built into the library instead of one
+ * the caller passes.  The pages have no counterpart; this is an interface
+ * convenience.
+ *   Workspace: one 8 MiB array per device, held from the library's load
+ *   until the process exits.  Calls whose pieces need more than that (G*k
+ *   entries of 4 + sizeof(elem) bytes each, plus 4*k bytes; see
+ *   ds_topk_long_row_workspace) return DS_EUNSUPPORTED before anything is
+ *   enqueued.  The call itself allocates nothing.
+ *   Sharing: every call on a device uses the same array and leaves its
+ *   contents behind; nothing in it needs to start at zero (each launch writes
+ *   what the next one reads).  Calls that overlap on the GPU (on different
+ *   streams, or from different host threads without ordering) race on the
+ *   array and give wrong results: order them on one stream.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (once per device, with that device current).  Make that first call
+ *   before capturing a CUDA graph that contains later calls.
+ */
+int ds_topk_long_row_noalloc(const void *x, int dtype, int64_t N, int k, int B, int B2,
+                             uint64_t seed, int32_t *out_idx, void *out_val, void *stream);
+
+/*
  * ds_topk_plan -- the launch plan ds_topk_ex would use on the current device
  * (x is only inspected for its alignment).  splits as in ds_topk_ex.
  */

@@ -148,6 +148,9 @@ def test_long_row_argument_errors(lib, args, status):
                               ctypes.c_uint64(0), FAKE, 1 << 20, a["out_idx"], a["out_val"], None)
     assert rc == status
     assert ds.ds_last_error_detail()
+    rc = lib.ds_topk_long_row_noalloc(a["x"], a["dtype"], a["N"], a["k"], a["B"], a["B2"],
+                                      ctypes.c_uint64(0), a["out_idx"], a["out_val"], None)
+    assert rc == status
     if a["x"] and a["out_idx"] and a["out_val"]:
         # the workspace query makes the same argument checks (it has no pointers)
         n = ctypes.c_size_t(0)

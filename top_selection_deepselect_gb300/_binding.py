@@ -22,8 +22,8 @@ DS_BF16 = 1
 DS_FP16 = 2
 
 ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_host_async", "ds_topk_long_row",
-                "ds_topk_long_row_workspace", "ds_topk_plan", "ds_topk_max_k", "ds_strerror",
-                "ds_last_error_detail"]
+                "ds_topk_long_row_workspace", "ds_topk_long_row_noalloc", "ds_topk_plan",
+                "ds_topk_max_k", "ds_strerror", "ds_last_error_detail"]
 
 
 class DSError(RuntimeError):
@@ -81,6 +81,8 @@ def load_library(path=None):
                                                    ctypes.POINTER(ctypes.c_int64),
                                                    ctypes.POINTER(ctypes.c_int)]
         lib.ds_topk_long_row_workspace.restype = i32
+        lib.ds_topk_long_row_noalloc.argtypes = [vp, i32, i64, i32, i32, i32, u64, vp, vp, vp]
+        lib.ds_topk_long_row_noalloc.restype = i32
         lib.ds_topk_plan.argtypes = [vp, i32, i32, i64, i32, i32, i32, i32,
                                      ctypes.POINTER(ds_plan_t)]
         lib.ds_topk_plan.restype = i32
@@ -156,6 +158,12 @@ def ds_topk_long_row_workspace(dtype, N, k, B, B2, plan=False):
                                                      ctypes.byref(P), ctypes.byref(G)),
            "ds_topk_long_row_workspace")
     return (n.value, P.value, G.value) if plan else n.value
+
+
+def ds_topk_long_row_noalloc(x, dtype, N, k, B, B2, seed, out_idx, out_val, stream):
+    return _check(load_library().ds_topk_long_row_noalloc(x, dtype, N, k, B, B2, _u64(seed),
+                                                           out_idx, out_val, stream),
+                  "ds_topk_long_row_noalloc")
 
 
 def ds_topk_plan(x, dtype, rows, N, k, B, B2, splits=0):

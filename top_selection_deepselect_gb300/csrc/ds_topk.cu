@@ -44,6 +44,7 @@ struct ClusterFit {
 
 struct DevInfo {
     bool ready = false;
+    unsigned char *noalloc_ws = nullptr;  // device address of g_noalloc_ws on this device
     ClusterFit fits[32];   // cached cluster-capacity answers (no query during graph capture)
     int nfits = 0;
     int sms = 0;
@@ -532,6 +533,32 @@ int long_row_plan(int dtype, int64_t N, int k, int B, RowPlan &rp)
     return row_plan(dtype, N, k, B, d->sms, rp);
 }
 
+// Workspace of ds_topk_long_row_noalloc: one fixed array per device that
+// loads the library, held until the process exits.  Every call shares it.
+constexpr size_t kNoAllocBytes = 8u << 20;
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocBytes];
+
+// The array's device address on the current device, looked up once per
+// device (host code cannot use the symbol itself as a device pointer).
+int noalloc_workspace(unsigned char **out)
+{
+    DevInfo *d = nullptr;
+    int dev = 0;
+    int rc = device_info(&d, &dev);
+    if (rc != DS_OK)
+        return rc;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->noalloc_ws == nullptr) {
+        void *ptr = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_ws);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaGetSymbolAddress(g_noalloc_ws)");
+        d->noalloc_ws = static_cast<unsigned char *>(ptr);
+    }
+    *out = d->noalloc_ws;
+    return DS_OK;
+}
+
 int long_row_run(const void *x, int dtype, int64_t N, int k, int B, int B2, uint64_t seed,
                  const RowPlan &rp, unsigned char *ws, int32_t *out_idx, void *out_val,
                  cudaStream_t stream)
@@ -677,6 +704,28 @@ int ds_topk_long_row(const void *x, int dtype, int64_t N, int k, int B, int B2, 
         return fail(DS_EINVAL, "workspace must be %zu-byte aligned", kWsAlign);
     return long_row_run(x, dtype, N, k, B, B2, seed, rp, static_cast<unsigned char *>(workspace),
                         out_idx, out_val, (cudaStream_t)stream);
+}
+
+int ds_topk_long_row_noalloc(const void *x, int dtype, int64_t N, int k, int B, int B2,
+                             uint64_t seed, int32_t *out_idx, void *out_val, void *stream)
+{
+    g_detail[0] = '\0';
+    int rc = long_row_check(x, dtype, N, k, B, B2, out_idx, out_val);
+    if (rc != DS_OK)
+        return rc;
+    RowPlan rp;
+    if ((rc = long_row_plan(dtype, N, k, B, rp)) != DS_OK)
+        return rc;
+    if (rp.bytes > kNoAllocBytes)
+        return fail(DS_EUNSUPPORTED,
+                    "the piece results need %zu bytes, more than the %zu-byte built-in workspace; "
+                    "use ds_topk_long_row with a workspace of your own",
+                    rp.bytes, kNoAllocBytes);
+    unsigned char *ws = nullptr;
+    if (rp.bytes > 0 && (rc = noalloc_workspace(&ws)) != DS_OK)
+        return rc;
+    return long_row_run(x, dtype, N, k, B, B2, seed, rp, ws, out_idx, out_val,
+                        (cudaStream_t)stream);
 }
 
 int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits,
