@@ -318,6 +318,75 @@ class Workload:
             raise self.ds.DSError(rc, "ds_topk", self.ds.ds_last_error_detail())
 
 
+class LongRowWorkload:
+    """One long row (ds_topk_long_row): replicas of the row and the launch
+    closure (three kernels per call: pieces, piece results, index gather)."""
+
+    def __init__(self, dev, torch, ds, l2_bytes):
+        self.c = c = workloads.LONG_ROW
+        self.name = "long_row_fp32"
+        self.ds = ds
+        bits, _ = workloads.generate(1, c["N"], c["dtype"], c["kind"], c["seed"])
+        one = torch.from_numpy(bits.reshape(-1).view(np.int32)).to(dev).view(torch.float32)
+        del bits
+        nbytes = one.numel() * 4
+        self.replicas = int(max(2, math.ceil(4 * l2_bytes / nbytes)))
+        self.l2_defeated = self.replicas * nbytes >= 4 * l2_bytes
+        self.x = torch.empty((self.replicas, c["N"]), dtype=torch.float32, device=dev)
+        self.x[:] = one
+        del one
+        self.rows = 1
+        self.read_bytes = workloads.algorithmic_bytes(c)
+        self.ws_bytes, self.piece_len, self.pieces = ds.ds_topk_long_row_workspace(
+            ds.DS_FP32, c["N"], c["k"], c["B"], c["B2"], plan=True)
+        self.ws = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
+        self.out_idx = torch.empty(c["k"], dtype=torch.int32, device=dev)
+        self.out_val = torch.empty(c["k"], dtype=torch.float32, device=dev)
+        self.launch(0, torch.cuda.current_stream(dev).cuda_stream)
+        torch.cuda.synchronize(dev)
+        ref = torch.topk(self.x[0], c["k"], largest=True, sorted=True).values
+        self.values_match_torch = bool(torch.equal(ref, self.out_val))
+
+    def launch(self, i, stream_handle):
+        import ctypes
+        c = self.c
+        lib = self.ds.load_library()
+        rc = lib.ds_topk_long_row(self.x[i % self.replicas].data_ptr(), self.ds.DS_FP32, c["N"],
+                                  c["k"], c["B"], c["B2"], ctypes.c_uint64(SEED),
+                                  self.ws.data_ptr(), self.ws_bytes, self.out_idx.data_ptr(),
+                                  self.out_val.data_ptr(), stream_handle)
+        if rc != 0:
+            raise self.ds.DSError(rc, "ds_topk_long_row", self.ds.ds_last_error_detail())
+
+
+def time_long_row(torch, ds, dev, l2, steps, warmup, peak, burn_seconds):
+    """The long-row workload: ds_topk_long_row against torch.topk (context)."""
+    wl = LongRowWorkload(dev, torch, ds, l2)
+    n = min(steps, 50)
+    ms = time_steps(torch, wl, n, warmup, burn_seconds=burn_seconds)
+    us = 1e3 * ms / n
+    gbs = wl.read_bytes / (us * 1e-6) / 1e9
+    x0 = wl.x[0]
+    for _ in range(2):
+        torch.topk(x0, wl.c["k"], largest=True, sorted=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(5):
+        torch.topk(wl.x[i % wl.replicas], wl.c["k"], largest=True, sorted=True)
+    e1.record()
+    e1.synchronize()
+    out = {"workload": wl.c["desc"], "entry_point": "ds_topk_long_row", "us_per_call": us,
+           "rows_per_s": 1.0 / (us * 1e-6), "gbs": gbs, "frac_of_measured_hbm": gbs / peak,
+           "algorithmic_bytes": wl.read_bytes, "pieces": wl.pieces, "piece_len": wl.piece_len,
+           "workspace_bytes": wl.ws_bytes, "kernels_per_call": 3,
+           "l2_defeated": wl.l2_defeated, "values_match_torch_topk": wl.values_match_torch,
+           "torch_topk": {"us_per_call": e0.elapsed_time(e1) * 1e3 / 5, "timing": "eager"}}
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
 def capture_graph(torch, wl, n, first):
     """A CUDA graph of n launches starting at replica index `first`."""
     g = torch.cuda.CUDAGraph()
@@ -574,6 +643,8 @@ def run_ours(args, rank, world):
                 del w2
                 torch.cuda.empty_cache()
         line["per_config"] = per
+        line["long_row"] = time_long_row(torch, ds, dev, l2, args.steps, args.warmup, peak,
+                                         args.burn_seconds)
         rate, dt, done, step_rows = oracle_rows_per_s(args.workload, seconds=args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": "%d rows of %s in %.1f s (rows cycled), single thread"
