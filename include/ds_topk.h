@@ -17,9 +17,12 @@
  * (section "算法": the block order must be random and independent of x), and
  * with it the amount of selection work and the counters of ds_topk_ex.
  *
- * Memory: every pointer passed to ds_topk / ds_topk_ex is device memory owned
- * by the caller.  The library allocates nothing on the device and keeps no
- * per-call state; it caches a few attributes per device.
+ * Memory: every pointer passed to ds_topk / ds_topk_ex / ds_topk_long_row is
+ * device memory owned by the caller.  The library allocates nothing on the
+ * device and keeps no per-call state; it caches a few attributes per device.
+ * The one device buffer it holds is the fixed 8 MiB workspace of
+ * ds_topk_long_row_noalloc, part of the library's image on every device that
+ * loads it.
  *
  * Layout: x is row-major with a row pitch of N elements; row r starts at
  * element r*N.  Outputs are row-major [rows][k].  Any alignment of x works;
