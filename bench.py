@@ -45,6 +45,7 @@ import workloads  # noqa: E402
 METRIC = "top-k rows/s and input-read HBM GB/s (fraction of GB300 peak) per config"
 UNIT = "rows/s"
 MAIN = "dsa_index_bf16"
+LONG_ROW_NAME = "long_row_fp32"
 SEED = 0x5EED5EED
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "top_selection_deepselect_gb300", "csrc", f)
@@ -58,7 +59,10 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=MAIN, choices=workloads.CONFIG_ORDER)
+    ap.add_argument("--workload", default=MAIN, choices=workloads.CONFIG_ORDER + [LONG_ROW_NAME],
+                    help="%s: one row over the whole GPU (ds_topk_long_row); the extras, the "
+                         "end-to-end number and the reference arm cover the matrix workloads "
+                         "only" % LONG_ROW_NAME)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip per-config lines, torch.topk and the CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -255,6 +259,8 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     name = args.workload
+    if name == LONG_ROW_NAME:
+        raise SystemExit("the reference arm times the matrix workloads; %s has none" % name)
     c = workloads.CONFIGS[name]
     rate, dt, done, step_rows = oracle_rows_per_s(name, steps=args.steps, warmup=args.warmup)
     sample = "%d steps x %d rows of %s (rows cycled), single thread" % (done, step_rows, name)
@@ -324,7 +330,7 @@ class LongRowWorkload:
 
     def __init__(self, dev, torch, ds, l2_bytes):
         self.c = c = workloads.LONG_ROW
-        self.name = "long_row_fp32"
+        self.name = LONG_ROW_NAME
         self.ds = ds
         bits, _ = workloads.generate(1, c["N"], c["dtype"], c["kind"], c["seed"])
         one = torch.from_numpy(bits.reshape(-1).view(np.int32)).to(dev).view(torch.float32)
@@ -336,9 +342,13 @@ class LongRowWorkload:
         self.x[:] = one
         del one
         self.rows = 1
+        self.esz = 4
         self.read_bytes = workloads.algorithmic_bytes(c)
         self.ws_bytes, self.piece_len, self.pieces = ds.ds_topk_long_row_workspace(
             ds.DS_FP32, c["N"], c["k"], c["B"], c["B2"], plan=True)
+        self.plan = {"entry_point": "ds_topk_long_row", "pieces": self.pieces,
+                     "piece_len": self.piece_len, "workspace_bytes": self.ws_bytes,
+                     "kernels_per_call": 3}
         self.ws = torch.empty(max(self.ws_bytes, 1), dtype=torch.uint8, device=dev)
         self.out_idx = torch.empty(c["k"], dtype=torch.int32, device=dev)
         self.out_val = torch.empty(c["k"], dtype=torch.float32, device=dev)
@@ -584,7 +594,11 @@ def run_ours(args, rank, world):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     peak, peak_kind = measured_peaks()
 
-    wl = Workload(args.workload, dev, torch, ds, l2)
+    long_row = args.workload == LONG_ROW_NAME
+    if long_row:
+        wl = LongRowWorkload(dev, torch, ds, l2)
+    else:
+        wl = Workload(args.workload, dev, torch, ds, l2)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -606,7 +620,7 @@ def run_ours(args, rank, world):
                           % (wl.replicas, wl.replicas * c["rows"] * c["N"] * wl.esz / 1e6,
                              l2 / 1e6),
                        parallelism="rows per rank, no exchange" if world > 1 else "1 GPU"),
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (3 if long_row else 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": profile_traffic(args.workload),
                      "peak_kind": peak_kind,
@@ -614,7 +628,12 @@ def run_ours(args, rank, world):
                      "kernel": "deepselect_topk_kernel"},
         "clocks": clocks,
     }
-    if rank == 0:
+    if long_row:
+        line["roofline"]["kernel"] = "ds_topk_long_row call (pieces, piece results, gather)"
+        line["e2e"] = None
+        line["note"] = ("long-row workload: achieved = the row's bytes / the whole call; no "
+                        "end-to-end number or extras")
+    if rank == 0 and not long_row:
         e2e_steps = args.e2e_steps or args.steps
         e2e_sync, h2d, d2h = time_e2e(torch, ds, wl, e2e_steps)
         e2e_pipe = time_e2e_pipelined(torch, ds, wl, e2e_steps, depth=E2E_DEPTH)
@@ -626,7 +645,7 @@ def run_ours(args, rank, world):
                                "steps may run concurrently" % (E2E_DEPTH, E2E_DEPTH),
                        "sync_per_step_value": e2e_sync * world,
                        "sync_per_step_path": "ds_topk_host, synchronised every step"}
-    if rank == 0 and world == 1 and not args.no_extras:
+    if rank == 0 and world == 1 and not args.no_extras and not long_row:
         line["torch_topk"] = time_torch_topk(torch, wl, args.steps)
         per = {}
         for name in workloads.CONFIG_ORDER:
