@@ -181,3 +181,53 @@ def test_long_row_workload_full_size():
     assert bool((val[:-1] >= val[1:]).all())
     tie = val[:-1] == val[1:]
     assert bool((idx[:-1][tie] < idx[1:][tie]).all())
+
+
+def topk_set_is_exact(x, idx, val, k):
+    """The outputs are exactly the row's top k under the total order (no NaN
+    or signed zero among the top values here): values are x[idx] and sorted,
+    indices are distinct, and #{x > v_k} + #{x == v_k, index <= i_k} == k."""
+    assert torch.equal(x[idx.long()], val)
+    assert len(torch.unique(idx)) == k
+    f = val.float()
+    assert bool((f[:-1] >= f[1:]).all())
+    tie = f[:-1] == f[1:]
+    assert bool((idx[:-1][tie] < idx[1:][tie]).all())
+    vk, ik = val[-1], int(idx[-1])
+    n_gt = int((x > vk).sum())
+    n_eq = int((x[:ik + 1] == vk).sum())
+    assert n_gt + n_eq == k
+
+
+def device_normal_bf16(n, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    x = torch.empty(n, dtype=torch.bfloat16, device=DEV)
+    step = 1 << 28
+    for s in range(0, n, step):
+        e = min(n, s + step)
+        x[s:e] = torch.randn(e - s, generator=g, device=DEV).to(torch.bfloat16)
+    return x
+
+
+def test_long_row_at_the_index_limit():
+    # N = 2^31 - 1 bf16 (4 GB): row indices up to 2^31 - 2 from piece * P + local
+    N, k = (1 << 31) - 1, 256
+    _, P, G = plan("bf16", N, k, 4096, 4096)
+    assert G > 1 and (G - 1) * P < N
+    x = device_normal_bf16(N, seed=67)
+    idx, val = ds.topk_long_row(x, k, 4096, 4096)
+    torch.cuda.synchronize()
+    topk_set_is_exact(x, idx, val, k)
+
+
+def test_matrix_rows_beyond_2_31_elements():
+    # 4200 rows of 2^19 bf16: rows from 4096 on start past element 2^31
+    rows, N, k = 4200, 1 << 19, 128
+    x = device_normal_bf16(rows * N, seed=68).view(rows, N)
+    idx, val = ds.topk(x, k, 1024, 1024)
+    ref = torch.topk(x, k, dim=-1, largest=True, sorted=True).values
+    torch.cuda.synchronize()
+    assert torch.equal(val, ref)
+    for r in (0, 4095, 4096, rows - 1):
+        topk_set_is_exact(x[r], idx[r], val[r], k)
