@@ -94,3 +94,35 @@ def test_edge_cases_pass_the_bounds_checks(lib, kind):
         assert check_word(lib) == 0, (k, B, B2, splits)
         np.testing.assert_array_equal(idx, ref_idx)
         np.testing.assert_array_equal(val, ref_val)
+
+
+@pytest.mark.parametrize("dtype,N,k,B,B2", [("fp32", 3_000_017, 512, 1024, 1024),
+                                            ("bf16", 1_048_577, 16, 8192, 1024)])
+def test_long_row_passes_the_bounds_checks(lib, dtype, N, k, B, B2):
+    # both launches of a long-row call, including a last piece shorter than P
+    lib.ds_topk_long_row_workspace.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p]
+    lib.ds_topk_long_row.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_uint64, ctypes.c_void_p,
+                                     ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+    code = {"fp32": 0, "bf16": 1}[dtype]
+    bits, _ = workloads.generate(1, N, dtype, "normal", seed=54)
+    x = torch.from_numpy(bits.reshape(-1).view(np.int32 if dtype == "fp32" else np.int16)).cuda()
+    nb, G = ctypes.c_size_t(0), ctypes.c_int(0)
+    assert lib.ds_topk_long_row_workspace(code, N, k, B, B2, ctypes.byref(nb), None,
+                                          ctypes.byref(G)) == 0
+    assert G.value > 1
+    ws = torch.empty(nb.value, dtype=torch.uint8, device="cuda")
+    oi = torch.empty(k, dtype=torch.int32, device="cuda")
+    ov = torch.empty(k, dtype=x.dtype, device="cuda")
+    check_word(lib)
+    rc = lib.ds_topk_long_row(x.data_ptr(), code, N, k, B, B2, ctypes.c_uint64(SEED),
+                              ws.data_ptr(), nb.value, oi.data_ptr(), ov.data_ptr(), None)
+    assert rc == 0, rc
+    torch.cuda.synchronize()
+    assert check_word(lib) == 0
+    ref_idx, ref_val = oracle.topk(bits, dtype, k)
+    np.testing.assert_array_equal(oi.cpu().numpy(), ref_idx[0])
+    np.testing.assert_array_equal(ov.cpu().numpy().view(bits.dtype), ref_val[0])

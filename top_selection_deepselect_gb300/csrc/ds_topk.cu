@@ -479,6 +479,8 @@ int row_plan(int dtype, int64_t N, int k, int B, int sms, RowPlan &rp)
         g = 2LL * sms;
     if (g >= 8)
         g = g / 8 * 8;
+    if (g < 2 && N > kMaxAutoSplits * kMaxPermBlocks * B)
+        g = 2;  // longer than one cluster's block orders hold: cut it anyway
     if (g < 2) {
         rp.G = 1;
         rp.P = N;
