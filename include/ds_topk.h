@@ -147,8 +147,9 @@ int ds_topk_host_async(const void *x_host, int dtype, int rows, const int32_t *r
  * results is selected by a second launch, and a gather maps the chosen
  * positions back to row indices (the multi-pass selection of one long row in
  * "CUDA 算子笔记 4", section "Top K Selection", takes the same place).  G
- * grows with N / k up to two pieces per SM; when it would be 1 the row is
- * selected directly and no workspace is used.
+ * grows with N / k up to two pieces per SM, and beyond that only when a
+ * piece would exceed the 4096 blocks one CTA orders; when it would be 1 the
+ * row is selected directly and no workspace is used.
  *   x          device, N elements of `dtype`
  *   N, k, B, B2, seed  as in ds_topk (rows = 1)
  *   workspace  caller-owned device memory, 256-byte aligned, of at least the
