@@ -231,3 +231,22 @@ def test_matrix_rows_beyond_2_31_elements():
     assert torch.equal(val, ref)
     for r in (0, 4095, 4096, rows - 1):
         topk_set_is_exact(x[r], idx[r], val[r], k)
+
+
+def test_refused_second_launch_enqueues_nothing():
+    # B = 16 makes 2048 pieces; their 2048 * 600 results are more blocks per
+    # slice than the second launch takes.  The call is refused before either
+    # launch: workspace and outputs keep what they held.
+    N, k, B = 1 << 27, 600, 16
+    nb, P, G = plan("fp32", N, k, B, B)
+    assert G * k // B > 16 * 4096
+    x = torch.zeros(N, dtype=torch.float32, device=DEV)
+    ws = torch.full((nb,), 0x5A, dtype=torch.uint8, device=DEV)
+    oi = torch.full((k,), -7, dtype=torch.int32, device=DEV)
+    ov = torch.full((k,), 3.0, dtype=torch.float32, device=DEV)
+    with pytest.raises(ds.DSError) as e:
+        ds.ds_topk_long_row(x.data_ptr(), 0, N, k, B, B, SEED, ws.data_ptr(), nb, oi.data_ptr(),
+                            ov.data_ptr(), None)
+    assert e.value.status == ds.DS_EUNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((ws == 0x5A).all()) and bool((oi == -7).all()) and bool((ov == 3.0).all())

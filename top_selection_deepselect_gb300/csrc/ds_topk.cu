@@ -356,9 +356,10 @@ int check_word(unsigned int **out)
 
 // `total` = elements in x when row_len is NULL (rows * N for a matrix; less
 // when the rows are consecutive pieces of one long row with a short last piece).
+// With enqueue = false every check and planning step runs and nothing is launched.
 int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int64_t total,
            int k, int B, int B2, uint64_t seed, int splits_req, int32_t *out_idx, void *out_val,
-           int64_t *stats, cudaStream_t stream)
+           int64_t *stats, cudaStream_t stream, bool enqueue = true)
 {
     int rc = check_args(x, dtype, rows, N, k, B, B2, splits_req, out_idx, out_val);
     if (rc != DS_OK)
@@ -395,6 +396,8 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     }
     if ((long long)rows * pl.p.splits > 0x7FFFFFFFLL)
         return fail(DS_EINVAL, "rows * splits exceeds the grid limit");
+    if (!enqueue)
+        return DS_OK;
     Params &p = pl.p;
     p.x = x;
     p.row_len = row_len;
@@ -571,14 +574,19 @@ int long_row_run(const void *x, int dtype, int64_t N, int k, int B, int B2, uint
     int32_t *idx1 = reinterpret_cast<int32_t *>(ws);
     void *val1 = ws + rp.off_val1;
     int32_t *q2 = reinterpret_cast<int32_t *>(ws + rp.off_q2);
-    int rc = launch(x, dtype, rp.G, nullptr, rp.P, N, k, B, B2, seed, 0, idx1, val1, nullptr,
-                    stream);
-    if (rc != DS_OK)
-        return rc;
-    rc = launch(val1, dtype, 1, nullptr, rp.N2, (int64_t)rp.G * k, k, B, B2, seed, 0, q2, out_val,
-                nullptr, stream);
-    if (rc != DS_OK)
-        return rc;
+    // both launches are planned before either is enqueued, so that a size
+    // the second one cannot take is reported with nothing enqueued
+    for (int pass = 0; pass < 2; ++pass) {
+        const bool enqueue = pass == 1;
+        int rc = launch(x, dtype, rp.G, nullptr, rp.P, N, k, B, B2, seed, 0, idx1, val1, nullptr,
+                        stream, enqueue);
+        if (rc != DS_OK)
+            return rc;
+        rc = launch(val1, dtype, 1, nullptr, rp.N2, (int64_t)rp.G * k, k, B, B2, seed, 0, q2,
+                    out_val, nullptr, stream, enqueue);
+        if (rc != DS_OK)
+            return rc;
+    }
     long_row_gather<<<(k + 255) / 256, 256, 0, stream>>>(q2, idx1, k, rp.P, out_idx);
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DS_OK : fail_cuda(e, "long_row_gather launch");
