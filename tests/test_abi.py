@@ -19,7 +19,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(ds_\w+)\s*\(", text, flags=re.M)))
 
@@ -45,7 +46,8 @@ def test_library_is_built_for_sm_103a(lib):
 def test_dtype_codes():
     # fp32, bf16 and IEEE fp16 are the dtypes of include/ds_topk.h
     assert (ds.DS_FP32, ds.DS_BF16, ds.DS_FP16) == (0, 1, 2)
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     assert "#define DS_FP16 2" in text
 
 

@@ -38,7 +38,7 @@ def _worker(rank, world, port, out):
 def test_reduce_over_ranks_two_processes():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:  # no fork of this multi-threaded process
         out = mgr.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
