@@ -49,8 +49,8 @@ LONG_ROW_NAME = "long_row_fp32"
 SEED = 0x5EED5EED
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = [os.path.join(ROOT, "top_selection_deepselect_gb300", "csrc", f)
-                  for f in ("ds_topk.cu", "ds_device.cuh", "ds_kernel.cuh", "ds_kernels_fp32.cu",
-                            "ds_kernels_bf16.cu")]
+                  for f in ("ds_topk.cu", "ds_device.cuh", "ds_kernel.cuh", "ds_stream.cuh",
+                            "ds_kernels_fp32.cu", "ds_kernels_bf16.cu", "ds_kernels_fp16.cu")]
 
 
 def parse_args():

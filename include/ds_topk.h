@@ -68,9 +68,13 @@ typedef struct {
     int warps_per_block;  /* warps filtering one B-block */
     int async_copy;       /* 1: 16-byte asynchronous copies into shared memory; 0: plain loads */
     int smem_bytes;       /* dynamic shared memory per CTA */
-    int capacity;         /* candidate-buffer capacity in entries (>= k + B + B2) */
+    int capacity;         /* candidate-buffer capacity in entries: >= k + B + B2 (kernel 0),
+                             >= k + B2 + one warp stage of 2 KiB (kernel 1) */
     int grid;             /* CTAs launched (rows * splits) */
     int ctas_per_sm;      /* resident CTAs per SM for this plan */
+    int kernel;           /* 0: block by block, the pages' loop step for step (counters);
+                             1: free-running warps (calls without counters whose rows take
+                             16-byte copies) */
 } ds_plan_t;
 
 /*

@@ -394,7 +394,11 @@ def test_plans_of_the_workloads():
         code = ds.DS_FP32 if c["dtype"] == "fp32" else ds.DS_BF16
         plan = ds.ds_topk_plan(1 << 20, code, c["rows"], c["N"], c["k"], c["B"], c["B2"], 0)
         assert plan["async_copy"] == 1
-        assert plan["capacity"] >= c["k"] + c["B"] + c["B2"]
+        # calls without counters take the free-running kernel; its buffer
+        # holds k + B2 plus one warp stage (2 KiB of elements)
+        assert plan["kernel"] == 1
+        esz = 4 if c["dtype"] == "fp32" else 2
+        assert plan["capacity"] >= c["k"] + c["B2"] + 2048 // esz
         assert plan["grid"] == c["rows"] * plan["splits"]
         s = plan["splits"]
         assert s & (s - 1) == 0 and s <= 16

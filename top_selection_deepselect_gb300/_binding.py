@@ -38,7 +38,7 @@ class DSError(RuntimeError):
 class ds_plan_t(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in
                 ("splits", "threads", "stages", "blocks_per_stage", "warps_per_block", "async_copy",
-                 "smem_bytes", "capacity", "grid", "ctas_per_sm")]
+                 "smem_bytes", "capacity", "grid", "ctas_per_sm", "kernel")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

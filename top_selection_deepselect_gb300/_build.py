@@ -10,6 +10,7 @@ LIB_PATH = os.path.join(PKG, "libds_topk.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("ds_topk.cu", "ds_kernels_fp32.cu", "ds_kernels_bf16.cu",
                                          "ds_kernels_fp16.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, "ds_device.cuh"), os.path.join(CSRC, "ds_kernel.cuh"),
+                  os.path.join(CSRC, "ds_stream.cuh"),
                   os.path.join(INCLUDE, "ds_topk.h")]
 
 # No fast-math and no flush-to-zero: the prefilter compares denormals exactly.

@@ -225,15 +225,17 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
 
-// Waits until at most `pending` (0..3) of this thread's newest commit groups
-// are still in flight.
+// Waits until at most `pending` (0..5; larger values wait as for 5) of this
+// thread's newest commit groups are still in flight.
 __device__ __forceinline__ void cp_async_wait_pending(int pending)
 {
     switch (pending) {
     case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
     case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
     case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
     }
 }
 
@@ -481,6 +483,8 @@ struct Misc {
     unsigned long long tslice[16];       // split rows: every slice's k-th composite (0: fewer than k)
     int pass;                            // select: digit passes so far (histogram rotation)
     unsigned long long tmin;             // select: smallest selected composite
+    int ctr[2];                          // free-running scan: buffer length, one word per epoch
+    __align__(16) int rem[kWarps];       // free-running scan: warp still has stages (at a sync point)
 };
 
 // Digit histograms: the register select uses one 256-bin histogram of 32-bit

@@ -61,6 +61,7 @@ struct Params {
     int stages;          // ring slots (1 for the plain-load path)
     int slot_bytes;      // bytes of one staged block (B * size rounded up to 16)
     int cpw;             // 16-byte chunks per warp of a block
+    int cap;             // candidate-buffer entries (free-running scan: overflow bound)
     int off_cand, off_perm, off_hist, off_holes, off_misc;
 };
 
@@ -781,8 +782,7 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
         for (int w = 0; w < warp; ++w)
             base += (int)ms->wsum[w];
         unsigned long long *dst = cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0);
-        const int mine_total = (int)mine;
-        if (DS_GUARD(ms, base + mine_total <= cand - reinterpret_cast<unsigned long long *>(ring), 32u))
+        if (DS_GUARD(ms, base + (int)mine <= cand - reinterpret_cast<unsigned long long *>(ring), 32u))
         for (int i0 = warp * 32; i0 < cnt; i0 += kThreads) {
             const int i = i0 + lane;
             const unsigned long long c = i < cnt ? cand[i] : 0ull;

@@ -1,5 +1,5 @@
-// ds_kernels_bf16.cu -- bf16 instantiations of the DeepSelect top-k kernel.
-#include "ds_kernel.cuh"
+// ds_kernels_bf16.cu -- bf16 instantiations of the DeepSelect top-k kernels.
+#include "ds_stream.cuh"
 
 namespace ds {
 
@@ -9,5 +9,7 @@ KernelFn kernel_bf16(bool async, bool wide)
         return wide ? deepselect_topk_kernel<1, true, 16> : deepselect_topk_kernel<1, true, 4>;
     return wide ? deepselect_topk_kernel<1, false, 16> : deepselect_topk_kernel<1, false, 4>;
 }
+
+KernelFn stream_kernel_bf16() { return deepselect_stream_kernel<1>; }
 
 }  // namespace ds

@@ -1,5 +1,5 @@
-// ds_kernels_fp16.cu -- IEEE fp16 instantiations of the DeepSelect top-k kernel.
-#include "ds_kernel.cuh"
+// ds_kernels_fp16.cu -- IEEE fp16 instantiations of the DeepSelect top-k kernels.
+#include "ds_stream.cuh"
 
 namespace ds {
 
@@ -9,5 +9,7 @@ KernelFn kernel_fp16(bool async, bool wide)
         return wide ? deepselect_topk_kernel<2, true, 16> : deepselect_topk_kernel<2, true, 4>;
     return wide ? deepselect_topk_kernel<2, false, 16> : deepselect_topk_kernel<2, false, 4>;
 }
+
+KernelFn stream_kernel_fp16() { return deepselect_stream_kernel<2>; }
 
 }  // namespace ds

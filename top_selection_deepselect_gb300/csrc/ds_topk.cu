@@ -1,7 +1,9 @@
 // ds_topk.cu -- host side of the DeepSelect top-k library: argument checks,
-// launch planning (split factor, ring depth, shared-memory layout) and the C
-// ABI declared in include/ds_topk.h.  The kernel itself is in ds_kernel.cuh,
-// instantiated per dtype in ds_kernels_fp32.cu, ds_kernels_bf16.cu and ds_kernels_fp16.cu.
+// launch planning (kernel, split factor, ring depth, shared-memory layout)
+// and the C ABI declared in include/ds_topk.h.  The kernels are in
+// ds_kernel.cuh (block by block, with counters) and ds_stream.cuh (free-running
+// warps), instantiated per dtype in ds_kernels_fp32.cu, ds_kernels_bf16.cu and
+// ds_kernels_fp16.cu.
 
 #include "ds_topk.h"
 
@@ -12,7 +14,7 @@
 #include <stdio.h>
 #include <string.h>
 
-#include "ds_kernel.cuh"
+#include "ds_stream.cuh"
 
 // ===========================================================================
 // Host side: argument checks, launch planning, C ABI.
@@ -92,19 +94,25 @@ int device_info(DevInfo **out, int *dev_out)
 
 using ds::KernelFn;
 
-// 12 instantiations: dtype x asynchronous copies x mask rounds (4 rounds cover
-// blocks of up to 2 KiB per warp, 16 up to 8 KiB per warp).
-KernelFn kernel_for(int dtype, bool async, bool wide, int *slot)
+// 15 instantiations: the block-by-block kernel per dtype x asynchronous
+// copies x mask rounds (4 rounds cover blocks of up to 2 KiB per warp, 16 up
+// to 8 KiB per warp), and the free-running kernel per dtype.
+KernelFn kernel_for(int dtype, bool stream, bool async, bool wide, int *slot)
 {
+    if (stream) {
+        *slot = 12 + dtype;
+        return dtype == DS_FP32 ? ds::stream_kernel_fp32()
+             : dtype == DS_BF16 ? ds::stream_kernel_bf16() : ds::stream_kernel_fp16();
+    }
     *slot = dtype * 4 + (async ? 2 : 0) + (wide ? 1 : 0);
     return dtype == DS_FP32 ? ds::kernel_fp32(async, wide)
          : dtype == DS_BF16 ? ds::kernel_bf16(async, wide) : ds::kernel_fp16(async, wide);
 }
 
-int ensure_attributes(DevInfo &d, int dtype, bool async, bool wide, KernelFn *fn)
+int ensure_attributes(DevInfo &d, int dtype, bool stream, bool async, bool wide, KernelFn *fn)
 {
     int slot = 0;
-    *fn = kernel_for(dtype, async, wide, &slot);
+    *fn = kernel_for(dtype, stream, async, wide, &slot);
     std::lock_guard<std::mutex> lock(g_mu);
     if (d.attr_set & (1u << slot))
         return DS_OK;
@@ -145,6 +153,8 @@ struct Plan {
     int smem;
     int ctas_per_sm;
     bool async;
+    bool stream;    // free-running kernel (no counters)
+    int per_chunk;  // elements per 16-byte chunk
 };
 
 
@@ -156,14 +166,20 @@ long long align128(long long v) { return (v + 127) / 128 * 128; }
 long long layout(Plan &pl, int stages, int splits)
 {
     Params &p = pl.p;
-    const long long ring_stream = (long long)stages * p.bps * p.slot_bytes;
+    const long long ring_stream = pl.stream ? (long long)ds::kWarps * stages * ds::kStageBytes
+                                            : (long long)stages * p.bps * p.slot_bytes;
     const long long ring_merge = splits > 1 ? (long long)splits * p.k * 8 : 0;
     long long off = align128(ring_stream > ring_merge ? ring_stream : ring_merge);
-    long long cap = (long long)p.k + p.B + p.B2;
+    // block by block: k + B + B2 (the largest length the loop reaches);
+    // free-running: k + B2 + one stage's elements (reservations beyond
+    // that are filled with the composite 0 and retried after a compaction)
+    long long cap = pl.stream ? (long long)p.k + p.B2 + (long long)ds::kStageChunks * pl.per_chunk
+                              : (long long)p.k + p.B + p.B2;
     if (cap < ds::pow2_ceil(p.k))
         cap = ds::pow2_ceil(p.k);
     if (cap < 32)
         cap = 32;
+    p.cap = (int)cap;
     p.off_cand = (int)off;
     off = align128(off + cap * 8);
     const long long m = (p.N + p.B - 1) / p.B;
@@ -202,6 +218,10 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     if (slot > 64 * 1024)
         return fail(DS_EUNSUPPORTED, "B * sizeof(elem) = %lld bytes exceeds 64 KiB", (long long)B * esz);
     pl.async = ((uintptr_t)x % 16 == 0) && ((N * esz) % 16 == 0) && (((long long)B * esz) % 16 == 0);
+    pl.per_chunk = 16 / esz;
+    // the free-running kernel serves every call without counters whose rows
+    // take 16-byte copies; counters follow the block-by-block loop exactly
+    pl.stream = !stats && pl.async;
     p.slot_bytes = (int)slot;
     int wpb = 1;
     while (wpb < ds::kWarps && p.slot_bytes / (wpb * 2) >= 2048)
@@ -264,7 +284,21 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     // ring depth: deepest that keeps two CTAs per SM, else deepest that fits
     int stages = 0;
     long long bytes = -1;
-    if (pl.async) {
+    if (pl.stream) {
+        for (int s = ds::kMaxStreamStages; s >= 2 && bytes < 0; --s) {
+            bytes = fits(s, splits, half_sm);
+            if (bytes >= 0)
+                stages = s;
+        }
+        for (int s = ds::kMaxStreamStages; s >= 2 && bytes < 0; --s) {
+            bytes = fits(s, splits, budget_one);
+            if (bytes >= 0)
+                stages = s;
+        }
+        if (bytes < 0)
+            pl.stream = false;  // the block-by-block kernel's smaller ring may fit
+    }
+    if (!pl.stream && pl.async) {
         for (int s = ds::kMaxStages; s >= 2 && bytes < 0; --s) {
             bytes = fits(s, splits, half_sm);
             if (bytes >= 0)
@@ -294,7 +328,6 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
     pl.ctas_per_sm = (int)((d.smem_per_sm) / (pl.smem + d.smem_reserved));
     if (pl.ctas_per_sm > 2048 / ds::kThreads)
         pl.ctas_per_sm = 2048 / ds::kThreads;
-    (void)stats;
     return DS_OK;
 }
 
@@ -375,7 +408,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     if ((rc = make_plan(x, dtype, rows, N, k, B, B2, splits_req, stats != nullptr, *d, pl)) != DS_OK)
         return rc;
     KernelFn fn = nullptr;
-    if ((rc = ensure_attributes(*d, dtype, pl.async, pl.p.cpw > 128, &fn)) != DS_OK)
+    if ((rc = ensure_attributes(*d, dtype, pl.stream, pl.async, pl.p.cpw > 128, &fn)) != DS_OK)
         return rc;
     // a cluster must fit on one GPC: shrink an automatic split factor until
     // the hardware can hold at least one cluster
@@ -761,9 +794,10 @@ int ds_topk_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, in
     plan->warps_per_block = pl.p.wpb;
     plan->async_copy = pl.async ? 1 : 0;
     plan->smem_bytes = pl.smem;
-    plan->capacity = (pl.p.off_perm - pl.p.off_cand) / 8;
+    plan->capacity = pl.p.cap;
     plan->grid = pl.grid;
     plan->ctas_per_sm = pl.ctas_per_sm;
+    plan->kernel = pl.stream ? 1 : 0;
     return DS_OK;
 }
 
