@@ -20,23 +20,19 @@ __global__ void k_scan(const uint32_t *in, int n, uint32_t *incl, uint32_t *excl
     }
 }
 
-// compaction as the select does it: keep flags per register slot, one
-// shared atomic per warp for the slots, ballot ranks for the positions
+// compaction as the select does it: keep flags per register slot, a warp
+// ballot count (the warp's slots start after the lower warps' counts; one
+// warp here), ballot ranks for the positions
 __global__ void k_compact(const uint32_t *x, const uint32_t *p, int n, unsigned long long *out,
                           int *count)
 {
-    __shared__ int fill;
     const int lane = threadIdx.x;
-    if (lane == 0)
-        fill = 0;
-    __syncwarp();
     uint32_t hi[1] = {0u}, lo[1] = {lane < n ? x[lane] : 0u};
     const uint32_t keep = (lane < n && p[lane]) ? 1u : 0u;
-    const int base = warp_reserve(keep, &fill, lane);
-    warp_scatter<1>(keep, hi, lo, out + base, lane);
-    __syncwarp();
+    const int total = warp_count<1>(keep);
+    warp_scatter<1>(keep, hi, lo, out, lane);
     if (lane == 0)
-        *count = fill;
+        *count = total;
 }
 
 // the mask walk of the append: lane 0 holds a bit mask of kept positions

@@ -282,6 +282,13 @@ __device__ __forceinline__ uint32_t lanemask_lt(int lane) { return (1u << lane) 
 // ---------------------------------------------------------------------------
 // 64-bit warp helpers.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long shfl_idx_u64(unsigned long long v, int src)
+{
+    const uint32_t lo = __shfl_sync(kFull, (uint32_t)v, src);
+    const uint32_t hi = __shfl_sync(kFull, (uint32_t)(v >> 32), src);
+    return ((unsigned long long)hi << 32) | lo;
+}
+
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m)
 {
     const uint32_t lo = __shfl_xor_sync(kFull, (uint32_t)v, m);
@@ -439,11 +446,18 @@ __device__ __forceinline__ void bitonic_sort_smem(unsigned long long *a, int P, 
 }
 
 // Sorts the cnt distinct entries a[0, cnt) ascending, in place (block
-// order); positions past cnt are left as they are.  Caller synchronises
+// order); positions past cnt are left as they are.  Up to 64 entries every
+// thread counts; up to 256 the complements are ranked in descending order
+// in `scratch` (256 entries;
+// the complement of a real entry is never 0, and 0 pads rank last) by
+// warp-sorted runs and binary searches; larger sets use the shared-memory
+// bitonic network in a itself (cap_pow2 entries).  Caller synchronises
 // before; ends synchronised.
-__device__ __forceinline__ void sort_asc_small(unsigned long long *a, int cnt, int cap_pow2)
+__device__ __forceinline__ void sort_asc_small(unsigned long long *a, int cnt, int cap_pow2,
+                                               unsigned long long *scratch)
 {
-    if (cnt <= kThreads) {
+    if (cnt <= 64) {
+        // few entries: every thread counts the entries below its own
         const int t = threadIdx.x;
         unsigned long long e = 0ull;
         int rank = 0;
@@ -455,6 +469,16 @@ __device__ __forceinline__ void sort_asc_small(unsigned long long *a, int cnt, i
         __syncthreads();
         if (t < cnt)
             a[rank] = e;
+        __syncthreads();
+    } else if (cnt <= kThreads) {
+        const int t = threadIdx.x;
+        scratch[t] = t < cnt ? ~a[t] : 0ull;
+        __syncthreads();
+        unsigned long long vals[1];
+        int ranks[1];
+        rank_desc_runs<1>(scratch, vals, ranks);
+        if (vals[0] != 0ull)
+            a[ranks[0]] = ~vals[0];
         __syncthreads();
     } else {
         for (int i = cnt + threadIdx.x; i < cap_pow2; i += kThreads)
@@ -474,15 +498,12 @@ struct Misc {
     __align__(16) int cntw[2][kWarps];   // survivors per warp, double-buffered
     uint32_t wsum[kWarps];               // per-warp totals of block scans
     uint32_t sel_digit, sel_above, sel_eq;
-    int group_count;
     int merge_count;                     // CTA 0 of a cluster: entries received
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
-    int fill;                            // select: slots handed out in the compaction
     unsigned int *check;                 // bounds-checked builds: violation bits (null otherwise)
     int runlen[16];                      // CTA 0 of a cluster: length of each slice's sorted run
     unsigned long long tslice[16];       // split rows: every slice's k-th composite (0: fewer than k)
     int pass;                            // select: digit passes so far (histogram rotation)
-    unsigned long long tmin;             // select: smallest selected composite
     int ctr[2];                          // free-running scan: buffer length, one word per epoch
     __align__(16) int rem[kWarps];       // free-running scan: warp still has stages (at a sync point)
 };
@@ -531,12 +552,14 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, Misc *ms)
 //     drop out.  Histogram buffers rotate over three, so clearing the next
 //     one needs no extra barrier.
 //  3. The loop stops when every entry of the chosen digit is needed, or when
-//     at most 32 remain tied; warp 0 then ranks the tied entries to find the
-//     exact k-th composite.
+//     at most 32 remain tied; the tied entries are gathered and every warp
+//     ranks them (shuffles) to find the exact k-th composite.
 //  4. Compaction: the selected entries of each register slot are counted by
-//     a warp ballot, one shared atomic per warp reserves their slots in
-//     cand[0, k), and the buffer is overwritten in place (all entries are in
-//     registers).
+//     a warp ballot; after one barrier every warp's slots in cand[0, k)
+//     start after those of the warps below it, and the buffer is overwritten
+//     in place (all entries are in registers).  Counts and minima travel
+//     through per-warp words rather than shared atomics, which serialise
+//     when eight warps hit one word.
 // ---------------------------------------------------------------------------
 // Warp 0's decision for one digit pass over histogram `hb`: lane l owns bins
 // 8l .. 8l+7; bins are ranked from the top.  Publishes the digit that holds
@@ -545,9 +568,12 @@ __device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, 
 {
     const uint4 q0 = *reinterpret_cast<const uint4 *>(hb + lane * 8);
     const uint4 q1 = *reinterpret_cast<const uint4 *>(hb + lane * 8 + 4);
-    // cu_t: entries in this lane's bins 8l+7 down to 8l+t
-    const uint32_t cu7 = q1.w, cu6 = cu7 + q1.z, cu5 = cu6 + q1.y, cu4 = cu5 + q1.x;
-    const uint32_t cu3 = cu4 + q0.w, cu2 = cu3 + q0.z, cu1 = cu2 + q0.y, cu0 = cu1 + q0.x;
+    // cu_t: entries in this lane's bins 8l+7 down to 8l+t (a sum tree, three
+    // dependent adds deep)
+    const uint32_t s76 = q1.w + q1.z, s54 = q1.y + q1.x, s32 = q0.w + q0.z, s10 = q0.y + q0.x;
+    const uint32_t s74 = s76 + s54, s30 = s32 + s10;
+    const uint32_t cu7 = q1.w, cu6 = s76, cu5 = s76 + q1.y, cu4 = s74;
+    const uint32_t cu3 = s74 + q0.w, cu2 = s74 + s32, cu1 = (s74 + s32) + q0.y, cu0 = s74 + s30;
     uint32_t suf = cu0;  // entries in the bins of this lane and all lanes above
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -559,13 +585,15 @@ __device__ __forceinline__ void digit_search(const uint32_t *hb, uint32_t need, 
     const bool found = excl < need && need <= suf;
     const uint32_t r = need - excl;
     // bins of this lane lying wholly above the need-th entry
-    const uint32_t nb = (uint32_t)(cu7 < r) + (uint32_t)(cu6 < r) + (uint32_t)(cu5 < r) +
-                        (uint32_t)(cu4 < r) + (uint32_t)(cu3 < r) + (uint32_t)(cu2 < r) +
-                        (uint32_t)(cu1 < r);
-    const uint32_t before = nb == 0 ? 0u : nb == 1 ? cu7 : nb == 2 ? cu6 : nb == 3 ? cu5
-                          : nb == 4 ? cu4 : nb == 5 ? cu3 : nb == 6 ? cu2 : cu1;
-    const uint32_t through = nb == 0 ? cu7 : nb == 1 ? cu6 : nb == 2 ? cu5 : nb == 3 ? cu4
-                           : nb == 4 ? cu3 : nb == 5 ? cu2 : nb == 6 ? cu1 : cu0;
+    const uint32_t nb = (((uint32_t)(cu7 < r) + (uint32_t)(cu6 < r)) +
+                         ((uint32_t)(cu5 < r) + (uint32_t)(cu4 < r))) +
+                        (((uint32_t)(cu3 < r) + (uint32_t)(cu2 < r)) + (uint32_t)(cu1 < r));
+    // before = cu_{8-nb} (0 for nb = 0), through = cu_{7-nb}: three levels of selects
+    const bool b0 = nb & 1u, b1 = nb & 2u, b2 = nb & 4u;
+    const uint32_t bA = b0 ? cu7 : 0u, bB = b0 ? cu5 : cu6, bC = b0 ? cu3 : cu4, bD = b0 ? cu1 : cu2;
+    const uint32_t before = b2 ? (b1 ? bD : bC) : (b1 ? bB : bA);
+    const uint32_t tA = b0 ? cu6 : cu7, tB = b0 ? cu4 : cu5, tC = b0 ? cu2 : cu3, tD = b0 ? cu0 : cu1;
+    const uint32_t through = b2 ? (b1 ? tD : tC) : (b1 ? tB : tA);
     if (found) {
         ms->sel_digit = 8u * (uint32_t)lane + 7u - nb;
         ms->sel_above = excl + before;
@@ -591,19 +619,6 @@ __device__ __forceinline__ int warp_count(uint32_t bits)
     for (int j = 0; j < R; ++j)
         tot += __popc(__ballot_sync(kFull, (bits >> j) & 1u));
     return tot;
-}
-
-// Slots for the entries flagged in `bits` (bit j = register slot j) of all
-// lanes: one shared atomic per warp on *counter; returns the warp's base.
-__device__ __forceinline__ int warp_reserve(uint32_t bits, int *counter, int lane)
-{
-    uint32_t tot = 0u;
-    for (uint32_t m = __reduce_or_sync(kFull, bits); m; m &= m - 1u)
-        tot += (uint32_t)__popc(__ballot_sync(kFull, (bits >> (__ffs(m) - 1)) & 1u));
-    int base = 0;
-    if (lane == 0 && tot)
-        base = atomicAdd(counter, (int)tot);
-    return __shfl_sync(kFull, base, 0);
 }
 
 // Writes the flagged entries to dst[0, count): slot by slot, each lane's
@@ -666,11 +681,6 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         ms->wand[warp] = ((unsigned long long)ah << 32) | al;
     }
     __syncthreads();  // also: all loads of cand are done, every warp read ms->pass
-    if (tid == 0) {
-        ms->group_count = 0;
-        ms->fill = 0;
-        ms->tmin = ~0ull;
-    }
     unsigned long long vo = 0ull, va = ~0ull;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
@@ -716,21 +726,28 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
         if (eq == need)
             break;
         if (eq <= 32u) {
-            // gather the tied entries; warp 0 ranks them
-            const int base = warp_reserve(live, &ms->group_count, lane);
-            if (DS_GUARD(ms, base + warp_count<R>(live) <= 32, 4u))
+            // gather the tied entries (each warp's at the offset of the
+            // warps below it) and let every warp rank them
+            const int mine = warp_count<R>(live);
+            if (lane == 0)
+                ms->wsum[warp] = (uint32_t)mine;
+            __syncthreads();
+            int base = 0;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w)
+                base += w < warp ? (int)ms->wsum[w] : 0;
+            if (DS_GUARD(ms, base + mine <= 32, 4u))
                 warp_scatter<R>(live, hi, lo, ms->group + base, lane);
             __syncthreads();
-            if (warp == 0) {
-                const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
-                uint32_t rank = 0;
-                for (uint32_t j = 0; j < eq; ++j)
-                    rank += ms->group[j] > g ? 1u : 0u;
-                if (lane < (int)eq && rank == need - 1u)
-                    ms->texact = g;
+            const unsigned long long g = lane < (int)eq ? ms->group[lane] : 0ull;
+            uint32_t rank = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const unsigned long long o = shfl_idx_u64(g, j);
+                rank += (j < (int)eq && o > g) ? 1u : 0u;
             }
-            __syncthreads();
-            texact = ms->texact;
+            const int src = __ffs(__ballot_sync(kFull, lane < (int)eq && rank == need - 1u)) - 1;
+            texact = shfl_idx_u64(g, src);
             exact = true;
             break;
         }
@@ -751,12 +768,15 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
     } else {
         sel |= live;
     }
-    const int cbase = warp_reserve(sel, &ms->fill, lane);
-    if (DS_GUARD(ms, cbase + warp_count<R>(sel) <= n, 2u))
-        warp_scatter<R>(sel, hi, lo, cand + cbase, lane);
+    // every warp's count (and smallest taken entry) goes to shared memory; the
+    // warp's slots start after those of the warps below it
+    const int mine = warp_count<R>(sel);
+    unsigned long long wmin = ~0ull;
     if (!exact) {
         // the chosen digit's entries are taken whole: the smallest of them
-        // is the k-th composite
+        // is the k-th composite.  A warp with no such entry reports the
+        // all-ones composite, which is below no entry (at most equal to a
+        // NaN at index 0), so it never changes the minimum.
         uint32_t mh = ~0u, ml = ~0u;
 #pragma unroll
         for (int j = 0; j < R; ++j)
@@ -768,15 +788,26 @@ static __device__ __noinline__ unsigned long long radix_select_regs(unsigned lon
             if (((live >> j) & 1u) && hi[j] == mh)
                 ml = min(ml, lo[j]);
         ml = __reduce_min_sync(kFull, ml);
-        // (a NaN key is all ones, so the sentinel cannot tell whether a lane
-        // holds entries)
-        if (__any_sync(kFull, live != 0u) && lane == 0)
-            atomicMin(&ms->tmin, ((unsigned long long)mh << 32) | ml);
+        wmin = ((unsigned long long)mh << 32) | ml;
+    }
+    if (lane == 0) {
+        ms->wsum[warp] = (uint32_t)mine;
+        ms->wmin[warp] = wmin;
     }
     if (tid == 0)
         ms->pass = pass;
     __syncthreads();
-    return exact ? texact : ms->tmin;
+    int cbase = 0;
+    unsigned long long tmin = ~0ull;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        cbase += w < warp ? (int)ms->wsum[w] : 0;
+        tmin = min_u64(tmin, ms->wmin[w]);
+    }
+    if (DS_GUARD(ms, cbase + mine <= n, 2u))
+        warp_scatter<R>(sel, hi, lo, cand + cbase, lane);
+    __syncthreads();
+    return exact ? texact : tmin;
 }
 
 // The same for sets too large for registers: every pass reads shared memory.
@@ -898,6 +929,16 @@ __device__ __forceinline__ unsigned long long radix_select_topk(unsigned long lo
     if (n <= 24 * kThreads)
         return radix_select_regs<24>(cand, n, k, hist, ms);
     return radix_select_smem(cand, n, k, hist, holes, ms);
+}
+
+// The select between streaming phases and at the end.  `room` = entries the
+// buffer at cand can hold (kept for selects that need scratch beyond n).
+__device__ __forceinline__ unsigned long long select_topk(unsigned long long *cand, int n, int k,
+                                                          int room, uint32_t *hist, uint16_t *holes,
+                                                          Misc *ms)
+{
+    (void)room;
+    return radix_select_topk(cand, n, k, hist, holes, ms);
 }
 
 }  // namespace ds

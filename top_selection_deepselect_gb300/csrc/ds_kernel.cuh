@@ -533,7 +533,8 @@ __device__ __forceinline__ bool bucket_sort_write(unsigned long long *arr, int c
 
 template <int DT>
 __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt, const Out &p, int row,
-                                               const unsigned char *xrow, uint32_t *scratch, Misc *ms)
+                                               const unsigned char *xrow, uint32_t *scratch, Misc *ms,
+                                               int room)
 {
     using E = Elem<DT>;
     const long long obase = (long long)row * p.k;
@@ -544,14 +545,29 @@ __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt,
         else
             reinterpret_cast<uint16_t *>(p.val)[obase + i] = (uint16_t)E::kNegInfBits;
     }
-    if (cnt <= kThreads) {
+    if (cnt <= kThreads && cnt > 64 && room >= kThreads) {
+        // ranks from warp-sorted runs and binary searches; with cnt > k only
+        // ranks below k are written, so this also selects
+        for (int i = cnt + threadIdx.x; i < kThreads; i += kThreads)
+            arr[i] = 0ull;
+        __syncthreads();
+        unsigned long long vals[1];
+        int ranks[1];
+        rank_desc_runs<1>(arr, vals, ranks);
+        if (vals[0] != 0ull && ranks[0] < p.k)
+            emit<DT>(p, obase, ranks[0], vals[0], xrow);
+    } else if (cnt <= kThreads) {
+        // every thread ranks one entry; with cnt > k only ranks below k are
+        // written, so this also selects
         const int t = threadIdx.x;
         if (t < cnt) {
             const unsigned long long e = arr[t];
             int rank = 0;
+#pragma unroll 8
             for (int j = 0; j < cnt; ++j)
                 rank += arr[j] > e ? 1 : 0;
-            emit<DT>(p, obase, rank, e, xrow);
+            if (rank < p.k)
+                emit<DT>(p, obase, rank, e, xrow);
         }
     } else if (cnt <= 1024) {
         if (!bucket_sort_write<DT>(arr, cnt, p, obase, xrow, scratch, ms)) {
@@ -692,17 +708,20 @@ __device__ __forceinline__ void merge_runs_and_write(unsigned long long *runs, i
 // ---------------------------------------------------------------------------
 template <int DT>
 static __device__ __noinline__ void finish_slice(const Out o, long long *stats, unsigned char *ring,
-                                                 unsigned long long *cand, uint32_t *whist,
+                                                 unsigned long long *cand, int room, uint32_t *whist,
                                                  uint16_t *holes, Misc *ms, int n, int S, int row,
                                                  int slice, const unsigned char *xrow, int A, int R,
                                                  int W, int peak)
 {
     const int tid = threadIdx.x;
     W += n;
+    // one CTA per row with at most one entry per thread: ranking the entries
+    // selects and orders them at once (sort_and_write)
+    const bool rank_all = S == 1 && n <= kThreads;
     unsigned long long tk = 0ull;  // this slice's k-th composite (0: fewer than k entries)
-    if (n > o.k)
-        tk = radix_select_topk(cand, n, o.k, whist, holes, ms);
-    const int cnt = n < o.k ? n : o.k;
+    if (n > o.k && !rank_all)
+        tk = select_topk(cand, n, o.k, room, whist, holes, ms);
+    const int cnt = rank_all ? n : (n < o.k ? n : o.k);
     if (stats != nullptr && tid == 0) {
         long long *s = stats + ((long long)row * S + slice) * 4;
         s[0] = A;
@@ -712,7 +731,7 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
     }
 
     if (S == 1) {
-        sort_and_write<DT>(cand, cnt, o, row, xrow, whist, ms);
+        sort_and_write<DT>(cand, cnt, o, row, xrow, whist, ms, room);
         return;
     }
 
@@ -800,8 +819,8 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
     const int kk = total < o.k ? total : o.k;
     unsigned long long *merged = reinterpret_cast<unsigned long long *>(ring);
     if (total > kk)
-        radix_select_topk(merged, total, kk, whist, holes, ms);
-    sort_and_write<DT>(merged, kk, o, row, xrow, whist, ms);
+        select_topk(merged, total, kk, (int)(cand - merged), whist, holes, ms);
+    sort_and_write<DT>(merged, kk, o, row, xrow, whist, ms, (int)(cand - merged));
 }
 
 // ---------------------------------------------------------------------------
@@ -845,15 +864,15 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
         }
         perm[i] = v;
     }
-    for (int i = tid; i < kHistWords; i += kThreads)
-        whist[i] = 0u;
     if (tid == 0) {
         ms->merge_count = 0;
         ms->pass = 0;
         ms->check = p.check;
     }
     __syncthreads();
-    sort_asc_small(perm, msl, P);
+    sort_asc_small(perm, msl, P, reinterpret_cast<unsigned long long *>(whist));  // histogram space as scratch
+    for (int i = tid; i < kHistWords; i += kThreads)
+        whist[i] = 0u;  // ordered before the first select by its barriers
 
     const int bps = p.bps;
     const int nst = (msl + bps - 1) / bps;
@@ -983,7 +1002,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
             W += n;
             R += 1;
             __syncthreads();  // every warp's appends are in the buffer
-            const unsigned long long tcomp = radix_select_topk(cand, n, p.k, whist, holes, ms);
+            const unsigned long long tcomp =
+                select_topk(cand, n, p.k, (p.off_perm - p.off_cand) >> 3, whist, holes, ms);
             n = p.k;
             thr = threshold_from<DT>(tcomp);
             gstart = trig + 1;
@@ -995,8 +1015,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
         cp_async_wait_pending(0);
     __syncthreads();  // appends of the last stage are visible
 
-    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, p.stats, ring, cand, whist, holes, ms, n, S, row,
-                     slice, xrow, A, R, W, peak);
+    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, p.stats, ring, cand, (p.off_perm - p.off_cand) >> 3,
+                     whist, holes, ms, n, S, row, slice, xrow, A, R, W, peak);
 }
 
 typedef void (*KernelFn)(Params);

@@ -114,6 +114,81 @@ __device__ __forceinline__ void stage_append(const unsigned char *sp, const Bloc
     }
 }
 
+// The first threshold for small k.  The pages start from -inf, so the first
+// k + B2 elements all enter the buffer and the first compaction selects
+// from them.  Any T with k elements of the row above it gives the same
+// answer, so here every lane takes the largest element of its chunks of
+// its warp's first kSeedStages stages (256 distinct elements of the row;
+// chunks not yet copied are left out), and T is placed just below the k-th
+// largest of these maxima: every element with that key passes, and the k maxima at or
+// above it guarantee k elements above T.  The k-th is found by ranking the 256
+// maxima (keys made distinct by the thread index; warp-sorted runs and
+// binary searches) in the candidate buffer, which is still empty.  Lanes without elements count as
+// key 0, below every element.  Called by all threads before the first
+// stage is consumed (its copies are waited for here).
+constexpr int kSeedMaxK = 128;
+#ifndef DS_SEED_STAGES
+#define DS_SEED_STAGES 4
+#endif
+constexpr int kSeedStages = DS_SEED_STAGES;  // stages per warp the maxima are taken over
+
+template <int DT>
+__device__ __forceinline__ uint32_t max_key_of(uint32_t mx)
+{
+    using E = Elem<DT>;
+    if (DT == 0)
+        return E::key(mx);
+    const uint32_t a = E::key(mx & 0xFFFFu), b = E::key(mx >> 16);
+    return a > b ? a : b;
+}
+
+template <int DT>
+__device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, const unsigned long long *perm,
+                                                 int msl, int len, int B, int k, int NS,
+                                                 unsigned long long *cand, Misc *ms)
+{
+    using E = Elem<DT>;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nseed = kSeedStages < NS - 1 ? kSeedStages : NS - 1;
+    cp_async_wait_pending(NS - 1 - nseed);  // this lane's copies of its first nseed stages landed
+    uint32_t mx = E::splat(E::kNegInfBits);
+    bool any = false;
+    int q = warp, pc = 0;  // the producer cursor's first steps
+    for (int st = 0; st < nseed && q < msl; ++st) {
+        const int lo = (int)(uint32_t)perm[q] * B;
+        const int nbytes = (min(lo + B, len) - lo) * E::kSize;
+        const int nch = (nbytes + 15) >> 4;
+        const int c0 = pc * kStageChunks;
+#pragma unroll
+        for (int i = 0; i < kLaneChunks; ++i) {
+            const int c = c0 + lane + 32 * i;
+            if ((c + 1) * 16 <= nbytes) {
+                mx = max_nan<DT>(mx, chunk_max<DT>(lds128(wring + st * kStageBytes + (lane + 32 * i) * 16)));
+                any = true;
+            }
+        }
+        if (c0 + kStageChunks >= nch) {
+            q += kWarps;
+            pc = 0;
+        } else {
+            ++pc;
+        }
+    }
+    const uint32_t key = any ? max_key_of<DT>(mx) : 0u;
+    cand[tid] = ((unsigned long long)key << 32) | (uint32_t)tid;
+    if (tid == 0)
+        ms->texact = 0ull;
+    __syncthreads();
+    unsigned long long vals[1];
+    int ranks[1];
+    rank_desc_runs<1>(cand, vals, ranks);  // the one 0 composite (thread 0 without elements) ranks last
+    if (ranks[0] == k - 1)
+        ms->texact = vals[0];
+    __syncthreads();  // texact is published
+    const uint32_t tkey = (uint32_t)(ms->texact >> 32);
+    return tkey == 0u ? threshold_initial<DT>() : threshold_from<DT>((unsigned long long)tkey << 32);
+}
+
 // grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.  Needs
 // 16-byte aligned rows and blocks (the planner checks).
 template <int DT>
@@ -155,8 +230,6 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         }
         perm[i] = v;
     }
-    for (int i = tid; i < kHistWords; i += kThreads)
-        whist[i] = 0u;
     if (tid == 0) {
         ms->merge_count = 0;
         ms->pass = 0;
@@ -165,7 +238,9 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         ms->ctr[1] = 0;
     }
     __syncthreads();
-    sort_asc_small(perm, msl, P);
+    sort_asc_small(perm, msl, P, reinterpret_cast<unsigned long long *>(whist));  // histogram space as scratch
+    for (int i = tid; i < kHistWords; i += kThreads)
+        whist[i] = 0u;  // ordered before the first select by its barriers
 
     const int NS = p.stages;
     unsigned char *wring = ring + (size_t)warp * NS * kStageBytes;
@@ -173,25 +248,40 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     const int trigger = p.k + p.B2;
     const int cap = p.cap;
 
-    // producer cursor: block order position and stage within the block
-    int pq = warp, pp = 0;
-    auto prefetch = [&](int slot) {
+    // Producer: block order position pq and stage pp within the block; the
+    // block's byte count and this lane's source address are set once per
+    // block.  Lane l copies the 16-byte chunks l, l+32, l+64, l+96 of a
+    // stage, at the same offsets of the slot.
+    int pq = warp, pp = 0, p_nbytes = 0;
+    const unsigned char *p_src = nullptr;
+    auto p_enter = [&]() {
         if (pq < msl) {
             const int lo = (int)(uint32_t)perm[pq] * B;
-            const int nbytes = (min(lo + B, len) - lo) * esz;
-            const int nch = (nbytes + 15) >> 4;
-            const int c0 = pp * kStageChunks;
-            unsigned char *dst = wring + slot * kStageBytes;
-            const unsigned char *src = xrow + (size_t)lo * esz;
+            p_nbytes = (min(lo + B, len) - lo) * esz;
+            p_src = xrow + (size_t)lo * esz + lane * 16;
+        }
+    };
+    p_enter();
+    const uint32_t ring_lane = smem_addr(wring) + lane * 16;
+    auto prefetch = [&](int slot) {
+        if (pq < msl) {
+            const int b0 = pp * kStageBytes;  // the stage's first byte in the block
+            const uint32_t dst = ring_lane + slot * kStageBytes;
+            const unsigned char *src = p_src + b0;
+            if (b0 + kStageBytes <= p_nbytes) {
 #pragma unroll
-            for (int i = 0; i < kLaneChunks; ++i) {
-                const int c = c0 + lane + 32 * i;
-                if ((c + 1) * 16 <= nbytes)
-                    cp_async16(smem_addr(dst + (lane + 32 * i) * 16), src + (size_t)c * 16);
+                for (int i = 0; i < kLaneChunks; ++i)
+                    cp_async16(dst + i * 512, src + i * 512);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kLaneChunks; ++i)
+                    if (b0 + (lane + 32 * i + 1) * 16 <= p_nbytes)
+                        cp_async16(dst + i * 512, src + i * 512);
             }
-            if (c0 + kStageChunks >= nch) {
+            if (b0 + kStageBytes >= p_nbytes) {
                 pq += kWarps;
                 pp = 0;
+                p_enter();
             } else {
                 ++pp;
             }
@@ -202,11 +292,22 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         prefetch(s);
 
     int ps = NS - 1;          // slot the next prefetch fills
-    int cq = warp, cpc = 0;   // consumer cursor
     int cs = 0;               // slot of the consumer's stage
     int epoch = 0;            // compactions so far (selects the length word)
     bool pending = false;     // the current stage waits for a compaction
+    // consumer: the same walk, with the block's bounds set once per block
+    int cq = warp, cpc = 0, c_lo = 0, c_hi = 0, c_nbytes = 0;
+    auto c_enter = [&]() {
+        if (cq < msl) {
+            c_lo = (int)(uint32_t)perm[cq] * B;
+            c_hi = min(c_lo + B, len);
+            c_nbytes = (c_hi - c_lo) * esz;
+        }
+    };
+    c_enter();
     Threshold thr = threshold_initial<DT>();
+    if (p.k <= kSeedMaxK && msl >= kWarps)
+        thr = seed_threshold<DT>(wring, perm, msl, len, B, p.k, NS, cand, ms);
 
     while (true) {
         while (cq < msl) {
@@ -217,39 +318,60 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                 ps = ps + 1 == NS ? 0 : ps + 1;
                 cp_async_wait_pending(NS - 1);  // this lane's copies of the stage landed
             }
-            BlockView bv;
-            bv.lo = (int)(uint32_t)perm[cq] * B;
-            bv.hi = min(bv.lo + B, len);
-            const int nbytes = (bv.hi - bv.lo) * esz;
-            const int nch = (nbytes + 15) >> 4;
-            bv.c0 = cpc * kStageChunks;
-            bv.c1 = min(bv.c0 + kStageChunks, nch);
-            bv.slot = nullptr;
+            const int b0 = cpc * kStageBytes;
             unsigned char *sp = wring + cs * kStageBytes;
-            // the partial last chunk of a row is loaded by the lane that filters it
-            if (!pending && (nbytes & 15) && nch - 1 < bv.c1 && ((nch - 1 - bv.c0) & 31) == lane) {
-                const int c = nch - 1;
-                unsigned char *dst = sp + (c - bv.c0) * 16;
-                for (int e = 0; e < kB; ++e) {
-                    const int j = bv.lo + c * kB + e;
-                    if (j < bv.hi) {
-                        if (DT == 0)
-                            reinterpret_cast<uint32_t *>(dst)[e] = reinterpret_cast<const uint32_t *>(xrow)[j];
-                        else
-                            reinterpret_cast<uint16_t *>(dst)[e] = reinterpret_cast<const uint16_t *>(xrow)[j];
+            // prefilter operand for the block's index range (see Threshold)
+            const bool ge = (uint32_t)c_lo < thr.ti;
+            BlockView bv;
+            bv.lo = c_lo;
+            bv.hi = c_hi;
+            bv.c0 = cpc * kStageChunks;
+            bv.t = ge ? thr.t_ge : thr.t_gt;
+            bv.refine = ge ? (thr.nan_ge || (uint32_t)c_hi > thr.ti) : thr.nan_gt;
+            bv.slot = nullptr;
+            uint32_t mword = 0u;
+            bool any;
+            if (b0 + kStageBytes <= c_nbytes && !bv.refine) {
+                // a whole stage (every chunk copied, no partial chunk) whose
+                // survivors need no per-element check: one maximum per lane
+                const unsigned char *lp = sp + lane * 16;
+                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512);
+                const uint4 v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
+                const uint32_t mx = max_nan<DT>(max_nan<DT>(chunk_max<DT>(v0), chunk_max<DT>(v1)),
+                                                max_nan<DT>(chunk_max<DT>(v2), chunk_max<DT>(v3)));
+                const bool pass = max_passes<DT>(mx, bv.t);
+                any = __any_sync(kFull, pass);
+                if (pass)
+                    mword = prefilter_bits<DT>(v0, bv.t) | (prefilter_bits<DT>(v1, bv.t) << kB) |
+                            (prefilter_bits<DT>(v2, bv.t) << (2 * kB)) |
+                            (prefilter_bits<DT>(v3, bv.t) << (3 * kB));
+            } else {
+                // the last stage of a row's last block, or a block that
+                // straddles T's index: chunk bounds and per-element checks
+                const int nch = (c_nbytes + 15) >> 4;
+                bv.c1 = min(bv.c0 + kStageChunks, nch);
+                // the partial last chunk of a row is loaded by the lane that filters it
+                if (!pending && (c_nbytes & 15) && nch - 1 < bv.c1 && ((nch - 1 - bv.c0) & 31) == lane) {
+                    const int c = nch - 1;
+                    unsigned char *dst = sp + (c - bv.c0) * 16;
+                    for (int e = 0; e < kB; ++e) {
+                        const int j = bv.lo + c * kB + e;
+                        if (j < bv.hi) {
+                            if (DT == 0)
+                                reinterpret_cast<uint32_t *>(dst)[e] = reinterpret_cast<const uint32_t *>(xrow)[j];
+                            else
+                                reinterpret_cast<uint16_t *>(dst)[e] = reinterpret_cast<const uint16_t *>(xrow)[j];
+                        }
                     }
                 }
+                const int slo = bv.lo + bv.c0 * kB;
+                const int shi = min(bv.lo + bv.c1 * kB, bv.hi);
+                bv.plain = !bv.refine && shi - slo == (bv.c1 - bv.c0) * kB;
+                mword = stage_filter<DT>(sp, bv, thr, lane);
+                any = __any_sync(kFull, mword != 0u);
             }
-            // prefilter operand for the stage's element range (see Threshold)
-            const int slo = bv.lo + bv.c0 * kB;
-            const int shi = min(bv.lo + bv.c1 * kB, bv.hi);
-            const bool ge = (uint32_t)slo < thr.ti;
-            bv.t = ge ? thr.t_ge : thr.t_gt;
-            bv.refine = ge ? (thr.nan_ge || (uint32_t)shi > thr.ti) : thr.nan_gt;
-            bv.plain = !bv.refine && shi - slo == (bv.c1 - bv.c0) * kB;
-            const uint32_t mword = stage_filter<DT>(sp, bv, thr, lane);
-            const int cnt = (int)__reduce_add_sync(kFull, (uint32_t)__popc(mword));
-            if (cnt) {
+            if (any) {
+                const int cnt = (int)__reduce_add_sync(kFull, (uint32_t)__popc(mword));
                 int base = 0;
                 if (lane == 0)
                     base = atomicAdd(&ms->ctr[epoch & 1], cnt);
@@ -266,9 +388,10 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                 stage_append<DT>(sp, bv, lane, mword, cand + base);
             }
             pending = false;
-            if (bv.c1 >= nch) {
+            if (b0 + kStageBytes >= c_nbytes) {
                 cq += kWarps;
                 cpc = 0;
+                c_enter();
             } else {
                 ++cpc;
             }
@@ -287,7 +410,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
             if (tid == 0)
                 ms->ctr[(epoch + 1) & 1] = p.k;  // ordered by the select's first barrier
             const unsigned long long tcomp =
-                radix_select_topk(cand, n_now < cap ? n_now : cap, p.k, whist, holes, ms);
+                select_topk(cand, n_now < cap ? n_now : cap, p.k, cap, whist, holes, ms);
             ++epoch;
             thr = threshold_from<DT>(tcomp);
             continue;
@@ -299,8 +422,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     const int n = ms->ctr[epoch & 1];
     __syncthreads();  // every thread read the length; this thread's copies have landed
 
-    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, nullptr, ring, cand, whist, holes, ms, n, S, row,
-                     slice, xrow, 0, 0, 0, 0);
+    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, nullptr, ring, cand, cap, whist, holes, ms, n, S,
+                     row, slice, xrow, 0, 0, 0, 0);
 }
 
 // Free-running kernel entry points of one dtype, defined in ds_kernels_<dtype>.cu.
