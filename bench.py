@@ -3,9 +3,10 @@
 
 One step = one ds_topk call over one batch of the workload (all rows): the
 random block order, the streaming filter, the in-loop radix selects, the
-split-row merge and the final sort.  The headline workload is the DSA
-index-score batch (64 rows x 32768 bf16, k = 512, B = B2 = 1024); the other
-workloads are reported under "per_config".
+split-row merge and the final sort.  The headline workload is the largest
+one that fits a GPU, the sampling-logit batch (256 rows x 128000 bf16,
+k = 50, B = B2 = 1024); the other workloads are reported under "per_config",
+each with the CPU oracle timed on a bounded sample of its rows.
 
 Timing: inputs are resident in HBM, rotated over enough replicas that the
 replicas together are at least four times the L2 size, so every step reads
@@ -16,9 +17,12 @@ points: pinned host input -> device -> top-k -> pinned host output every
 step, four steps in flight on four streams (ds_topk_host_async), and also
 synchronised every step (ds_topk_host).
 
-Multi-GPU (torchrun): every rank runs its own full batch (weak scaling, no
-data exchange); rank 0 prints the total rows of all ranks over the slowest
-rank's time.
+Multi-GPU (torchrun): rows are independent, so the batch is partitioned into
+contiguous row ranges (row_range), one per rank; every rank selects its own
+rows and writes its own slice of the outputs, with no data exchange.  By
+default (--scaling weak) the batch holds `rows` rows per rank; with
+--scaling strong the workload's rows are split across the ranks.  Rank 0
+prints the total rows of all ranks over the slowest rank's time.
 
 --impl reference times the CPU oracle (single thread, the plain definition
 by full sort) on the same workload, each step a bounded sample of rows.
@@ -44,7 +48,7 @@ import workloads  # noqa: E402
 
 METRIC = "top-k rows/s and input-read HBM GB/s (fraction of GB300 peak) per config"
 UNIT = "rows/s"
-MAIN = "dsa_index_bf16"
+MAIN = "sampling_logits_bf16"
 LONG_ROW_NAME = "long_row_fp32"
 SEED = 0x5EED5EED
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -69,6 +73,10 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
     ap.add_argument("--burn-seconds", type=float, default=0.5,
                     help="extra untimed back-to-back warm-up before the timed region")
+    ap.add_argument("--scaling", choices=["weak", "strong"], default="weak",
+                    help="weak: every rank selects `rows` rows of a batch of rows x ranks; "
+                         "strong: the workload's rows are split across the ranks")
+    ap.add_argument("--cpu-seconds-per-config", type=float, default=3.0)
     return ap.parse_args()
 
 
@@ -98,10 +106,16 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def profile_traffic(workload):
+def kernel_name(plan):
+    """The kernel a call with this plan launches (calls without counters use
+    the free-running kernel when their rows take 16-byte copies)."""
+    return "deepselect_stream_kernel" if plan and plan.get("kernel") == 1 else "deepselect_topk_kernel"
+
+
+def profile_traffic(workload, kernel):
     """DRAM bytes per launch from the committed ncu summary of this workload,
     if it was taken on the current kernel sources."""
-    path = os.path.join(PROFILE_DIR, "deepselect_topk_kernel__%s.txt" % workload)
+    path = os.path.join(PROFILE_DIR, "%s__%s.txt" % (kernel, workload))
     if not os.path.exists(path):
         return None
     fields = {}
@@ -168,9 +182,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def rank_rows(rank, world, rows, scaling):
+    """This rank's contiguous row range [r0, r1) of the batch and the batch's
+    row count: weak scaling gives every rank `rows` rows of a batch of
+    rows * world, strong scaling splits `rows` (row_range of the package)."""
+    import top_selection_deepselect_gb300 as ds
+    total = rows * world if scaling == "weak" else rows
+    r0, r1 = ds.row_range(rank, world, total)
+    return r0, r1, total
+
+
 def reduce_over_ranks(ms, rows, dist, device="cpu"):
-    """Slowest rank's time and the rows all ranks processed (weak scaling:
-    every rank runs its own batch; nothing but these two numbers is exchanged)."""
+    """Slowest rank's time and the rows all ranks processed (each rank selects
+    its own row range; nothing but these two numbers is exchanged)."""
     if dist is None:
         return ms, rows
     import torch
@@ -194,6 +218,16 @@ def cfg_desc(c, name, plan=None):
     if plan:
         d["plan"] = plan
     return d
+
+
+def data_desc(name):
+    """What the synthetic rows stand in for (no public dataset is named)."""
+    what = {"small_fp32": "a small score row", "dsa_index_bf16": "DSA index scores",
+            "dsa_decode_ragged_fp32": "DSA long-context decode scores",
+            "sampling_logits_bf16": "sampling logits",
+            "adversarial_fp32": "adversarially ordered and heavily tied rows",
+            LONG_ROW_NAME: "one long score row"}.get(name, name)
+    return "synthetic (seeded; stands in for %s)" % what
 
 
 # ---------------------------------------------------------------------------
@@ -268,7 +302,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(done, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": c["dtype"], "data": "synthetic (seeded; stands in for DSA index scores)",
+        "dtype": c["dtype"], "data": data_desc(name),
         "config": cfg_desc(c, name),
         "cpu_baseline": {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": sample, "host": host_cpu()},
@@ -281,9 +315,11 @@ def run_reference(args, rank, world):
 # our arm
 # ---------------------------------------------------------------------------
 class Workload:
-    """Device-resident replicas of one workload plus the launch closure."""
+    """Device-resident replicas of one workload plus the launch closure.
+    `local_rows` = the rows [lr0, lr1) of the workload this rank selects
+    (all of them unless the rows are split across ranks)."""
 
-    def __init__(self, name, dev, torch, ds, l2_bytes, max_bytes=8 << 30):
+    def __init__(self, name, dev, torch, ds, l2_bytes, max_bytes=8 << 30, local_rows=None):
         self.name = name
         self.c = c = workloads.CONFIGS[name]
         self.torch = torch
@@ -304,10 +340,12 @@ class Workload:
         self.rl = None if row_len is None else torch.from_numpy(row_len).to(dev)
         self.out_idx = torch.empty((c["rows"], c["k"]), dtype=torch.int32, device=dev)
         self.out_val = torch.empty((c["rows"], c["k"]), dtype=tdt, device=dev)
-        self.rows = c["rows"]
-        self.read_bytes = workloads.algorithmic_bytes(name, row_len=row_len)
-        self.plan = ds.ds_topk_plan(self.x.data_ptr(), self.code, c["rows"], c["N"], c["k"],
-                                    c["B"], c["B2"], 0)
+        self.lr0, self.lr1 = local_rows if local_rows is not None else (0, c["rows"])
+        self.rows = self.lr1 - self.lr0
+        self.read_bytes = workloads.algorithmic_bytes(
+            name, row_len=None if row_len is None else row_len[self.lr0:self.lr1], rows=self.rows)
+        self.plan = ds.ds_topk_plan(self.x.data_ptr(), self.code, max(self.rows, 1), c["N"],
+                                    c["k"], c["B"], c["B2"], 0)
         # one eager call first: attribute set-up and cluster checks happen outside any capture
         self.launch(0, torch.cuda.current_stream(dev).cuda_stream)
         torch.cuda.synchronize(dev)
@@ -316,10 +354,11 @@ class Workload:
         c = self.c
         lib = self.ds.load_library()
         import ctypes
-        rc = lib.ds_topk(self.x[i % self.replicas].data_ptr(), self.code, c["rows"],
-                         None if self.rl is None else self.rl.data_ptr(), c["N"], c["k"], c["B"],
-                         c["B2"], ctypes.c_uint64(SEED), self.out_idx.data_ptr(),
-                         self.out_val.data_ptr(), stream_handle)
+        a, b = self.lr0, self.lr1
+        rc = lib.ds_topk(self.x[i % self.replicas, a:b].data_ptr(), self.code, b - a,
+                         None if self.rl is None else self.rl[a:b].data_ptr(), c["N"], c["k"],
+                         c["B"], c["B2"], ctypes.c_uint64(SEED), self.out_idx[a:b].data_ptr(),
+                         self.out_val[a:b].data_ptr(), stream_handle)
         if rc != 0:
             raise self.ds.DSError(rc, "ds_topk", self.ds.ds_last_error_detail())
 
@@ -595,10 +634,16 @@ def run_ours(args, rank, world):
     peak, peak_kind = measured_peaks()
 
     long_row = args.workload == LONG_ROW_NAME
+    batch_rows = None
     if long_row:
         wl = LongRowWorkload(dev, torch, ds, l2)
     else:
-        wl = Workload(args.workload, dev, torch, ds, l2)
+        rows = workloads.CONFIGS[args.workload]["rows"]
+        r0, r1, batch_rows = rank_rows(rank, world, rows, args.scaling)
+        # weak: this rank's slice of the batch is a full copy of the workload's
+        # rows; strong: it is the rows [r0, r1) of the workload itself
+        local = (0, rows) if args.scaling == "weak" else (r0, r1)
+        wl = Workload(args.workload, dev, torch, ds, l2, local_rows=local)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
@@ -613,19 +658,21 @@ def run_ours(args, rank, world):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": c["dtype"],
-        "data": "synthetic (seeded; stands in for DSA index scores)",
+        "scaling": args.scaling, "vs_baseline": None, "dtype": c["dtype"],
+        "data": data_desc(args.workload),
         "config": dict(cfg_desc(c, args.workload, wl.plan),
                        l2="inputs rotated over %d device replicas (%.0f MB >= 4x L2 %.0f MB)"
                           % (wl.replicas, wl.replicas * c["rows"] * c["N"] * wl.esz / 1e6,
                              l2 / 1e6),
-                       parallelism="rows per rank, no exchange" if world > 1 else "1 GPU"),
+                       parallelism=("contiguous row ranges of a %d-row batch, one per rank, no "
+                                    "exchange" % batch_rows) if world > 1 else "1 GPU"),
         "gpu_launches": args.steps * (3 if long_row else 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profile_traffic(args.workload),
+                     "frac": achieved / peak,
+                     "traffic": None if long_row else profile_traffic(args.workload, kernel_name(wl.plan)),
                      "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": wl.read_bytes,
-                     "kernel": "deepselect_topk_kernel"},
+                     "kernel": None if long_row else kernel_name(wl.plan)},
         "clocks": clocks,
     }
     if long_row:
@@ -658,6 +705,13 @@ def run_ours(args, rank, world):
                          "l2_defeated": w2.l2_defeated,
                          "algorithmic_bytes": w2.read_bytes, "plan": w2.plan,
                          "torch_topk": time_torch_topk(torch, w2, args.steps)}
+            if name != args.workload:
+                rate, dt, done, step_rows = oracle_rows_per_s(
+                    name, seconds=args.cpu_seconds_per_config, rows_per_step=1)
+                per[name]["cpu_baseline"] = {
+                    "value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+                    "sample": "%d rows of %s in %.1f s (rows cycled), single thread"
+                              % (done * step_rows, name, dt)}
             if w2 is not wl:
                 del w2
                 torch.cuda.empty_cache()

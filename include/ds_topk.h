@@ -114,6 +114,25 @@ int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64
                int64_t *stats, void *stream);
 
 /*
+ * ds_topk_stats_order -- ds_topk_ex with counters and a chosen block order,
+ * for studying the scan's work (a diagnostic; the result is the same).
+ *   order   DS_ORDER_RANDOM: the random order of ds_topk_ex (the method);
+ *           DS_ORDER_IDENTITY: blocks in index order.  DeepSelect-deep-dive,
+ *           section "算法", requires an order that is random and independent
+ *           of x: on a row sorted ascending, index order makes every block
+ *           beat the threshold, so every element is appended and the work W
+ *           grows with the row instead of staying within the bound of
+ *           section "RadixSelectTopK 总处理元素数的期望上界".
+ *   stats   required (non-NULL when rows > 0), as in ds_topk_ex; splits >= 1.
+ * Other arguments and errors as ds_topk_ex; DS_EINVAL for another order.
+ */
+#define DS_ORDER_RANDOM 0
+#define DS_ORDER_IDENTITY 1
+int ds_topk_stats_order(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N,
+                        int k, int B, int B2, uint64_t seed, int splits, int order,
+                        int32_t *out_idx, void *out_val, int64_t *stats, void *stream);
+
+/*
  * ds_topk_host -- the same operation on HOST buffers.
  *   x_host, row_len_host (nullable), out_idx_host, out_val_host: host memory
  *   (page-locked memory gives asynchronous copies; pageable memory works).

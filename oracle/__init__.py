@@ -78,6 +78,8 @@ def _bind(lib):
                                     ctypes.c_uint64, ctypes.c_int, ctypes.c_int, c_i32p,
                                     ctypes.c_void_p, c_i64p]
     lib.ds_oracle_model.restype = ctypes.c_int
+    lib.ds_oracle_sweep_f32.argtypes = []
+    lib.ds_oracle_sweep_f32.restype = ctypes.c_int64
     return lib
 
 

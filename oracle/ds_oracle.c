@@ -104,6 +104,61 @@ uint32_t ds_oracle_key_f16(uint32_t bits16)
     return bits | 0x8000u;
 }
 
+/* Exhaustive check of ds_oracle_key_f32 over all 2^32 bit patterns against
+ * C's own float comparison (IEEE 754, no fast-math): every non-NaN pattern is
+ * visited in increasing numeric order -- negative patterns from -inf
+ * (0xFF800000) down to -0 (0x80000000), then positive ones from +0 up to
+ * +inf (0x7F800000) -- and each step must be numerically increasing as C
+ * floats (or -0 to +0, which compare equal) with the key increasing in the
+ * same way (equal exactly at -0 -> +0); every NaN pattern must map to the
+ * largest key, above the key of +inf.  Returns the number of violations. */
+int64_t ds_oracle_sweep_f32(void)
+{
+    int64_t bad = 0;
+    uint32_t prev_bits = 0xFF800000u, prev_key = ds_oracle_key_f32(prev_bits);
+    float prev_f;
+    memcpy(&prev_f, &prev_bits, 4);
+    uint32_t bits = 0xFF800000u;
+    for (int half = 0; half < 2; ++half) {
+        for (;;) {
+            if (half == 0) {
+                if (bits == 0x80000000u)
+                    break;
+                --bits;                       /* next negative pattern toward -0 */
+            } else {
+                bits = bits == 0x80000000u ? 0u : bits + 1u;
+            }
+            float f;
+            memcpy(&f, &bits, 4);
+            const uint32_t key = ds_oracle_key_f32(bits);
+            const int same = prev_bits == 0x80000000u && bits == 0u;  /* -0 -> +0 */
+            if (same) {
+                if (!(f == prev_f) || key != prev_key)
+                    ++bad;
+            } else if (!(prev_f < f) || !(prev_key < key)) {
+                ++bad;
+            }
+            prev_bits = bits;
+            prev_key = key;
+            prev_f = f;
+            if (half == 1 && bits == 0x7F800000u)
+                break;
+        }
+    }
+    const uint32_t inf_key = ds_oracle_key_f32(0x7F800000u);
+    for (uint32_t m = 0x7F800001u; m <= 0x7FFFFFFFu; ++m) {
+        float f;
+        memcpy(&f, &m, 4);
+        if (f == f)                           /* C must agree that it is a NaN */
+            ++bad;
+        if (ds_oracle_key_f32(m) != 0xFFFFFFFFu || ds_oracle_key_f32(m | 0x80000000u) != 0xFFFFFFFFu)
+            ++bad;
+    }
+    if (!(inf_key < 0xFFFFFFFFu))
+        ++bad;
+    return bad;
+}
+
 static int dtype_known(int dtype)
 {
     return dtype == DS_ORACLE_FP32 || dtype == DS_ORACLE_BF16 || dtype == DS_ORACLE_FP16;

@@ -88,6 +88,17 @@ def test_argument_errors_are_reported_before_any_launch(lib, args, status):
     assert ds.ds_last_error_detail()
 
 
+@pytest.mark.parametrize("order,stats,splits", [(2, FAKE, 1), (-1, FAKE, 1), (0, None, 1),
+                                                (1, None, 1), (1, FAKE, 0)])
+def test_block_order_entry_checks_its_arguments(lib, order, stats, splits):
+    """ds_topk_stats_order: a known order, counters (the order changes only
+    them) and an explicit split factor, all refused before any launch."""
+    rc = lib.ds_topk_stats_order(FAKE, ds.DS_FP32, 4, None, 1024, 8, 128, 128, ctypes.c_uint64(1),
+                                 splits, order, FAKE, FAKE, stats, None)
+    assert rc == ds.DS_EINVAL
+    assert ds.ds_last_error_detail()
+
+
 def test_zero_rows_is_a_noop(lib):
     assert lib.ds_topk(None, ds.DS_BF16, 0, None, 100, 5, 16, 16, ctypes.c_uint64(0),
                        None, None, None) == ds.DS_OK

@@ -139,6 +139,35 @@ def test_stats_match_model(name, splits):
         assert np.all(peak <= c["k"] + c["B2"] + c["B"] - 1)
 
 
+def test_identity_order_blows_up_the_work_on_ascending_rows():
+    """DeepSelect-deep-dive, "算法": the block order must be random and
+    independent of the data.  On the adversarial workload's ascending rows,
+    index order (ds_topk_stats_order) makes every block beat the threshold:
+    every element is appended and W is many times the random order's.  Both
+    orders' counters equal the step-by-step model's for the same order, and
+    the result is the oracle's either way."""
+    c = workloads.CONFIGS["adversarial_fp32"]
+    bits, _ = workloads.config_inputs("adversarial_fp32")
+    bits = np.ascontiguousarray(bits[:16])  # rows 0..15: sorted ascending
+    k, B, B2 = c["k"], c["B"], c["B2"]
+    ref_idx, ref_val = oracle.topk(bits, "fp32", k)
+    x = to_device(bits, "fp32")
+    W = {}
+    for order in (ds.DS_ORDER_RANDOM, ds.DS_ORDER_IDENTITY):
+        out = ds.topk(x, k, B, B2, seed=SEED, splits=1, stats=True, order=order)
+        torch.cuda.synchronize()
+        idx, val, st = out[0].cpu().numpy(), val_bits(out[1], "fp32"), out[2].cpu().numpy()
+        assert_same(idx, val, ref_idx, ref_val)
+        _, _, m_stats = oracle.model(bits, "fp32", k, B, B2, SEED, splits=1,
+                                     identity_order=order == ds.DS_ORDER_IDENTITY)
+        np.testing.assert_array_equal(st, m_stats)
+        W[order] = st[:, 0, 2]
+    n = bits.shape[1]
+    A_id = st[:, 0, 0]
+    assert np.all(A_id == n)  # index order on ascending rows: every element is appended
+    assert np.all(W[ds.DS_ORDER_IDENTITY] >= 10 * W[ds.DS_ORDER_RANDOM])
+
+
 # ---------------------------------------------------------------------------
 # Edge cases.
 # ---------------------------------------------------------------------------

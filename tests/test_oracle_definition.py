@@ -278,6 +278,13 @@ def test_fp16_key_map_exhaustive():
     np.testing.assert_array_equal(np.argsort(k, kind="stable"), np.argsort(k32, kind="stable"))
 
 
+def test_fp32_key_map_exhaustive():
+    """All 2^32 fp32 patterns (oracle sweep in C): walked in increasing
+    numeric order as C floats compare them, the key increases with them,
+    equal only at -0 -> +0; every NaN pattern maps to the largest key."""
+    assert oracle.load().ds_oracle_sweep_f32() == 0
+
+
 def test_fp32_key_map_sampled_and_edges():
     rng = np.random.default_rng(1)
     edges = np.array([0, 0x80000000, 1, 0x80000001, 0x007FFFFF, 0x807FFFFF, 0x00800000,

@@ -71,6 +71,27 @@ def test_no_alloc_entry_point_matches_the_workspace_entry_point(ds):
                            ref_v.view(torch.int16 if dtype != "fp32" else torch.int32))
 
 
+def test_no_alloc_entry_point_on_a_row_selected_directly(ds):
+    """A row shorter than 64 k is selected in one piece (G = 1): no workspace
+    is needed, the built-in array is not used, and the result still equals
+    the caller-workspace entry point's."""
+    lib = ds.load_library()
+    N, k = 5000, 100
+    x = device_input(N, "fp32", "normal", 74)
+    nb, P, G = ds.ds_topk_long_row_workspace(0, N, k, 1024, 1024, plan=True)
+    assert G == 1 and nb == 0 and P == N
+    ref_i, ref_v = with_workspace(ds, x, 0, k, 1024, 1024)
+    for _ in range(2):
+        oi = torch.full((k,), -7, dtype=torch.int32, device=DEV)
+        ov = torch.zeros(k, dtype=torch.float32, device=DEV)
+        rc = lib.ds_topk_long_row_noalloc(x.data_ptr(), 0, N, k, 1024, 1024, ctypes.c_uint64(SEED),
+                                          oi.data_ptr(), ov.data_ptr(), None)
+        assert rc == 0, ds.ds_last_error_detail()
+        torch.cuda.synchronize()
+        assert torch.equal(oi, ref_i)
+        assert torch.equal(ov.view(torch.int32), ref_v.view(torch.int32))
+
+
 def test_no_alloc_entry_point_refuses_more_than_its_workspace(ds):
     lib = ds.load_library()
     N, k = 1 << 26, 4096

@@ -20,8 +20,10 @@ DS_ECUDA = -3
 DS_FP32 = 0
 DS_BF16 = 1
 DS_FP16 = 2
+DS_ORDER_RANDOM = 0
+DS_ORDER_IDENTITY = 1
 
-ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_host", "ds_topk_host_async", "ds_topk_long_row",
+ENTRY_POINTS = ["ds_topk", "ds_topk_ex", "ds_topk_stats_order", "ds_topk_host", "ds_topk_host_async", "ds_topk_long_row",
                 "ds_topk_long_row_workspace", "ds_topk_long_row_noalloc", "ds_topk_plan",
                 "ds_topk_max_k", "ds_strerror", "ds_last_error_detail"]
 
@@ -67,6 +69,9 @@ def load_library(path=None):
         lib.ds_topk.restype = i32
         lib.ds_topk_ex.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, i32, vp, vp, vp, vp]
         lib.ds_topk_ex.restype = i32
+        lib.ds_topk_stats_order.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, i32, i32,
+                                            vp, vp, vp, vp]
+        lib.ds_topk_stats_order.restype = i32
         lib.ds_topk_host.argtypes = [vp, i32, i32, vp, i64, i32, i32, i32, u64, vp, vp,
                                      vp, vp, vp, vp, vp]
         lib.ds_topk_host.restype = i32
@@ -126,6 +131,26 @@ def ds_topk_ex(x, dtype, rows, row_len, N, k, B, B2, seed, splits, out_idx, out_
     return _check(load_library().ds_topk_ex(x, dtype, rows, row_len, N, k, B, B2, _u64(seed),
                                              splits, out_idx, out_val, stats, stream),
                   "ds_topk_ex")
+
+
+def ds_topk_stats_order(x, dtype, rows, row_len, N, k, B, B2, seed, splits, order, out_idx,
+                        out_val, stats, stream):
+    return _check(load_library().ds_topk_stats_order(x, dtype, rows, row_len, N, k, B, B2,
+                                                      _u64(seed), splits, order, out_idx, out_val,
+                                                      stats, stream),
+                  "ds_topk_stats_order")
+
+
+def row_range(rank, world, rows):
+    """Contiguous rows [r0, r1) of `rows` that rank `rank` of `world` selects
+    when a batch is split across GPUs: rows are independent, so every rank
+    calls ds_topk on its own slice and writes its own slice of the outputs;
+    the first rows % world ranks take one row more."""
+    if world < 1 or not 0 <= rank < world or rows < 0:
+        raise ValueError("need 0 <= rank < world and rows >= 0")
+    base, extra = divmod(rows, world)
+    r0 = rank * base + min(rank, extra)
+    return r0, r0 + base + (1 if rank < extra else 0)
 
 
 def ds_topk_host(x_host, dtype, rows, row_len_host, N, k, B, B2, seed, out_idx_host,
@@ -201,11 +226,13 @@ def dtype_code(t):
 
 
 def topk(x, k, B, B2, seed=0x5EED5EED, row_len=None, splits=0, stats=False, out_idx=None,
-         out_val=None, stream=None):
+         out_val=None, stream=None, order=None):
     """Top-k of every row of a 2-D CUDA tensor x (float32, bfloat16 or float16).
 
     Returns (idx int32 [rows, k], val [rows, k]) and, with stats=True, also an
-    int64 [rows, splits, 4] tensor of (A, R, W, peak) per slice.
+    int64 [rows, splits, 4] tensor of (A, R, W, peak) per slice.  `order`
+    (DS_ORDER_RANDOM or DS_ORDER_IDENTITY, with stats=True) calls
+    ds_topk_stats_order.
     """
     import torch
     if x.dim() != 2 or not x.is_cuda:
@@ -230,9 +257,16 @@ def topk(x, k, B, B2, seed=0x5EED5EED, row_len=None, splits=0, stats=False, out_
         st_t = torch.zeros((rows, splits, 4), dtype=torch.int64, device=x.device)
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    ds_topk_ex(x.data_ptr(), code, rows, rl_ptr, N, k, B, B2, seed, splits,
-               out_idx.data_ptr(), out_val.data_ptr(),
-               None if st_t is None else st_t.data_ptr(), stream.cuda_stream)
+    if order is not None:
+        if not stats:
+            raise ValueError("order needs stats=True")
+        ds_topk_stats_order(x.data_ptr(), code, rows, rl_ptr, N, k, B, B2, seed, splits, order,
+                            out_idx.data_ptr(), out_val.data_ptr(), st_t.data_ptr(),
+                            stream.cuda_stream)
+    else:
+        ds_topk_ex(x.data_ptr(), code, rows, rl_ptr, N, k, B, B2, seed, splits,
+                   out_idx.data_ptr(), out_val.data_ptr(),
+                   None if st_t is None else st_t.data_ptr(), stream.cuda_stream)
     if stats:
         return out_idx, out_val, st_t
     return out_idx, out_val

@@ -62,6 +62,7 @@ struct Params {
     int slot_bytes;      // bytes of one staged block (B * size rounded up to 16)
     int cpw;             // 16-byte chunks per warp of a block
     int cap;             // candidate-buffer entries (free-running scan: overflow bound)
+    int identity;        // block-by-block kernel: visit blocks in index order (diagnostic)
     int off_cand, off_perm, off_hist, off_holes, off_misc;
 };
 
@@ -859,7 +860,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
         unsigned long long v = ~0ull;
         if (i < msl) {
             const uint32_t b = (uint32_t)(first_block + i);
-            const uint32_t w = philox_word0(b, (uint32_t)row, (uint32_t)slice, 0u, p.seed_lo, p.seed_hi);
+            const uint32_t w =
+                p.identity ? 0u : philox_word0(b, (uint32_t)row, (uint32_t)slice, 0u, p.seed_lo, p.seed_hi);
             v = ((unsigned long long)w << 32) | b;
         }
         perm[i] = v;

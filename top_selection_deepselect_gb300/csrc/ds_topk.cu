@@ -392,7 +392,7 @@ int check_word(unsigned int **out)
 // With enqueue = false every check and planning step runs and nothing is launched.
 int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N, int64_t total,
            int k, int B, int B2, uint64_t seed, int splits_req, int32_t *out_idx, void *out_val,
-           int64_t *stats, cudaStream_t stream, bool enqueue = true)
+           int64_t *stats, cudaStream_t stream, bool enqueue = true, int order = DS_ORDER_RANDOM)
 {
     int rc = check_args(x, dtype, rows, N, k, B, B2, splits_req, out_idx, out_val);
     if (rc != DS_OK)
@@ -446,6 +446,7 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     p.check = nullptr;
 #endif
     p.seed_hi = (uint32_t)(seed >> 32);
+    p.identity = order == DS_ORDER_IDENTITY ? 1 : 0;
 
     cudaLaunchConfig_t cfg;
     memset(&cfg, 0, sizeof(cfg));
@@ -644,6 +645,19 @@ int ds_topk_ex(const void *x, int dtype, int rows, const int32_t *row_len, int64
     g_detail[0] = '\0';
     return launch(x, dtype, rows, row_len, N, (int64_t)rows * N, k, B, B2, seed, splits, out_idx,
                   out_val, stats, (cudaStream_t)stream);
+}
+
+int ds_topk_stats_order(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N,
+                        int k, int B, int B2, uint64_t seed, int splits, int order,
+                        int32_t *out_idx, void *out_val, int64_t *stats, void *stream)
+{
+    g_detail[0] = '\0';
+    if (order != DS_ORDER_RANDOM && order != DS_ORDER_IDENTITY)
+        return fail(DS_EINVAL, "order = %d is not DS_ORDER_RANDOM (0) or DS_ORDER_IDENTITY (1)", order);
+    if (!stats && rows > 0)
+        return fail(DS_EINVAL, "stats must be non-NULL: the block order only changes the counters");
+    return launch(x, dtype, rows, row_len, N, (int64_t)rows * N, k, B, B2, seed, splits, out_idx,
+                  out_val, stats, (cudaStream_t)stream, true, order);
 }
 
 static int host_call(const void *x_host, int dtype, int rows, const int32_t *row_len_host, int64_t N,
