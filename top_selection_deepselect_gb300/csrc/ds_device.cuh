@@ -239,6 +239,21 @@ __device__ __forceinline__ void cp_async_wait_pending(int pending)
     }
 }
 
+// Programmatic dependent launch: let the next grid on the stream be
+// scheduled now (its CTAs start once this grid's CTAs have all started and
+// wait in dependent_grid_wait), and wait until the previous grid on the
+// stream has completed and its memory is visible.  Both are no-ops for a
+// launch without the programmatic attribute.
+__device__ __forceinline__ void allow_dependent_grid()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void dependent_grid_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint4 lds128(const unsigned char *p)
 {
     return *reinterpret_cast<const uint4 *>(p);

@@ -830,6 +830,8 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
 template <int DT, bool ASYNC, int MAXR>
 __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Params p)
 {
+    allow_dependent_grid();
+    dependent_grid_wait();  // before the first read of x, row_len or the outputs
     using E = Elem<DT>;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

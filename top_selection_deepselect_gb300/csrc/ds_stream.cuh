@@ -194,6 +194,8 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Params p)
 {
+    allow_dependent_grid();
+    dependent_grid_wait();  // before the first read of x, row_len or the outputs
     using E = Elem<DT>;
     constexpr int kB = E::kPerChunk;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -311,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
 
     while (true) {
         while (cq < msl) {
+            const int b0 = cpc * kStageBytes;
+            // prefilter operand for the block's index range (see Threshold)
+            const bool ge = (uint32_t)c_lo < thr.ti;
             if (!pending) {
                 if (ld_volatile_shared(&ms->ctr[epoch & 1]) >= trigger)
                     break;  // a compaction is due
@@ -318,10 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                 ps = ps + 1 == NS ? 0 : ps + 1;
                 cp_async_wait_pending(NS - 1);  // this lane's copies of the stage landed
             }
-            const int b0 = cpc * kStageBytes;
             unsigned char *sp = wring + cs * kStageBytes;
-            // prefilter operand for the block's index range (see Threshold)
-            const bool ge = (uint32_t)c_lo < thr.ti;
             BlockView bv;
             bv.lo = c_lo;
             bv.hi = c_hi;
