@@ -35,7 +35,6 @@ import os
 import platform
 import subprocess
 import sys
-import tempfile
 import time
 
 import numpy as np
@@ -60,7 +59,9 @@ KERNEL_SOURCES = [os.path.join(ROOT, "top_selection_deepselect_gb300", "csrc", f
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=5000,
+                    help="timed steps (the default keeps the timed region long enough for "
+                         "clock samples to fall inside it)")
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=MAIN, choices=workloads.CONFIG_ORDER + [LONG_ROW_NAME],
@@ -70,7 +71,7 @@ def parse_args():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip per-config lines, torch.topk and the CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
+    ap.add_argument("--e2e-steps", type=int, default=200, help="0: same as --steps")
     ap.add_argument("--burn-seconds", type=float, default=0.5,
                     help="extra untimed back-to-back warm-up before the timed region")
     ap.add_argument("--scaling", choices=["weak", "strong"], default="weak",
@@ -133,41 +134,53 @@ def profile_traffic(workload, kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling in a child process (our own PID)."""
+    """nvidia-smi clock / throttle samples taken by a background thread while
+    the GPU works: one complete query per call (no streamed output that a
+    terminated child could leave unflushed), every ~50 ms."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index):
         self.index = index
-        self.proc = None
-        self.file = None
+        self.rows = []
+        self.thread = None
+        self.stop_flag = False
+
+    def _query(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                               timeout=10)
+            return [l.strip().split(", ") for l in r.stdout.splitlines() if l.strip()]
+        except Exception:
+            return []
+
+    def _loop(self):
+        while not self.stop_flag:
+            self.rows.extend(self._query())
+            time.sleep(0.05)
 
     def start(self):
-        try:
-            self.file = tempfile.TemporaryFile(mode="w+")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=self.file, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
-        time.sleep(0.3)
+        import threading
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        t0 = time.perf_counter()
+        while not self.rows and time.perf_counter() - t0 < 5.0:  # the sampler is running
+            time.sleep(0.02)
 
     def stop(self):
-        if self.proc is None:
+        if self.thread is None:
             return None
-        time.sleep(0.1)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.file.seek(0)
-        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        n_before = len(self.rows)
+        t0 = time.perf_counter()
+        while len(self.rows) == n_before and time.perf_counter() - t0 < 2.0:
+            time.sleep(0.02)  # at least one sample after the timed steps were enqueued
+        self.stop_flag = True
+        self.thread.join(timeout=15)
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        for r in self.rows:
             try:
                 sm.append(float(r[1]))
                 smax.append(float(r[2]))
@@ -296,8 +309,9 @@ def run_reference(args, rank, world):
     if name == LONG_ROW_NAME:
         raise SystemExit("the reference arm times the matrix workloads; %s has none" % name)
     c = workloads.CONFIGS[name]
-    rate, dt, done, step_rows = oracle_rows_per_s(name, steps=args.steps, warmup=args.warmup)
-    sample = "%d steps x %d rows of %s (rows cycled), single thread" % (done, step_rows, name)
+    rate, dt, done, step_rows = oracle_rows_per_s(name, steps=args.steps, warmup=args.warmup,
+                                                  rows_per_step=1)
+    sample = "%d steps x %d row of %s (rows cycled), single thread" % (done, step_rows, name)
     line = {
         "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / max(done, 1),
