@@ -51,6 +51,21 @@ __global__ void k_mask_walk(const uint32_t *x, uint32_t mask, uint32_t *out, int
     *count = pos;
 }
 
+// the free-running kernel's block order: position q -> block id, for q < n
+__global__ void k_block_order(uint32_t n, uint32_t word, uint32_t *out)
+{
+    BlockOrder order;
+    order.init(n, word);
+    for (uint32_t q = blockIdx.x * blockDim.x + threadIdx.x; q < n; q += gridDim.x * blockDim.x)
+        out[q] = order(q);
+}
+
+extern "C" int prim_block_order(uint32_t n, uint32_t word, uint32_t *out)
+{
+    k_block_order<<<64, 256>>>(n, word, out);
+    return (int)cudaDeviceSynchronize();
+}
+
 extern "C" int prim_scan(const uint32_t *in, int n, uint32_t *incl, uint32_t *excl)
 {
     k_scan<<<1, 32>>>(in, n, incl, excl);

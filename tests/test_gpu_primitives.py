@@ -43,6 +43,7 @@ def lib(tmp_path_factory):
     lib.prim_scan.argtypes = [vp, i32, vp, vp]
     lib.prim_compact.argtypes = [vp, vp, i32, vp, vp]
     lib.prim_mask_walk.argtypes = [vp, u32, vp, vp]
+    lib.prim_block_order.argtypes = [u32, u32, vp]
     return lib
 
 
@@ -82,3 +83,32 @@ def test_ffs_mask_walk_matches_the_pages_example(lib):
     assert lib.prim_mask_walk(x.data_ptr(), mask, out.data_ptr(), count.data_ptr()) == 0
     n = int(count.item())
     assert out[:n].cpu().tolist() == g["output"]
+
+
+def test_block_order_is_a_permutation(lib):
+    """The free-running kernel's block order (keyed Feistel network, cycle
+    walked) maps the positions 0..n-1 onto the block ids 0..n-1 exactly once,
+    for sizes around powers of four (the network's domains) and several keys."""
+    for n in [1, 2, 3, 4, 5, 15, 16, 17, 31, 63, 64, 65, 125, 255, 256, 257, 1000, 1024, 1025,
+              4095, 4096, 65537]:
+        for word in [0, 1, 0x5EED5EED, 0xFFFFFFFF]:
+            out = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+            assert lib.prim_block_order(n, word, out.data_ptr()) == 0
+            got = np.sort(out.cpu().numpy())
+            np.testing.assert_array_equal(got, np.arange(n, dtype=np.int32))
+
+
+def test_block_order_spreads_positions(lib):
+    """Where block 0 lands over many keys: its mean position is near the middle
+    (the order depends on the key, not on the data), and the keys give
+    different orders."""
+    n = 125
+    pos0, firsts = [], set()
+    for word in range(400):
+        out = torch.empty(n, dtype=torch.int32, device="cuda")
+        assert lib.prim_block_order(n, word * 2654435761 % (1 << 32), out.data_ptr()) == 0
+        o = out.cpu().numpy()
+        pos0.append(int(np.nonzero(o == 0)[0][0]))
+        firsts.add(int(o[0]))
+    assert abs(np.mean(pos0) - (n - 1) / 2) < 8  # 400 draws: standard error about 1.8
+    assert len(firsts) > 60

@@ -206,6 +206,65 @@ __device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint3
 }
 
 // ---------------------------------------------------------------------------
+// A keyed pseudorandom permutation of [0, n), evaluated per position without
+// a table (the free-running kernel needs the block at a position without
+// sorting the whole order first).  A balanced Feistel network of 4 rounds on
+// 2h bits, 2^(2h) >= n: (L, R) -> (R, L ^ F(R ^ key_r)), F multiplying by
+// odd constants with xor-shifts, is a permutation of [0, 2^(2h)); positions
+// that map past n are walked on along their cycle ("cycle walking"), which
+// returns below n at the latest when it comes back to the start, so the
+// result is a bijection of [0, n).  Keys come from one Philox word per row
+// slice, so the order is random and independent of the data.
+// ---------------------------------------------------------------------------
+struct BlockOrder {
+    uint32_t n, h, mask;
+    uint32_t key[4];
+
+    __device__ __forceinline__ static uint32_t mix(uint32_t x)
+    {
+        x *= 0xD2511F53u;
+        x ^= x >> 15;
+        x *= 0xCD9E8D57u;
+        x ^= x >> 13;
+        return x;
+    }
+
+    __device__ __forceinline__ void init(uint32_t count, uint32_t word)
+    {
+        n = count;
+        h = 0;
+        while (h < 16 && (1u << (2 * h)) < count)
+            ++h;
+        mask = (1u << h) - 1u;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            key[r] = mix(word + (uint32_t)r * 0x9E3779B9u);
+    }
+
+    __device__ __forceinline__ uint32_t operator()(uint32_t q) const
+    {
+        if (n <= 1u)
+            return 0u;
+        uint32_t x = q;
+        const unsigned long long domain = 1ull << (2 * h);
+        for (unsigned long long walk = 0; walk < domain; ++walk) {
+            uint32_t L = x >> h, R = x & mask;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t f = mix(R ^ key[r]) & mask;
+                const uint32_t t = R;
+                R = L ^ f;
+                L = t;
+            }
+            x = (L << h) | R;
+            if (x < n)
+                break;
+        }
+        return x;
+    }
+};
+
+// ---------------------------------------------------------------------------
 // PTX wrappers: shared-memory address, asynchronous copies, 128-bit loads.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void *p)

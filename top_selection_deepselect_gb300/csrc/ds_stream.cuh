@@ -8,6 +8,9 @@
 // shrinks it to k and raises T.  Any T that is at most the row's k-th
 // element gives the same answer (the result is unique under the total
 // order), so this kernel lets the eight warps of a CTA run independently:
+//   * the block order is a keyed pseudorandom permutation (BlockOrder);
+//     every warp evaluates its own positions in parallel across its lanes,
+//     so it issues its first copies at once, with no CTA-wide sort first;
 //   * warp w scans the blocks at positions w, w + 8, w + 16, ... of the
 //     CTA's block order, in stages of 2 KiB (128 chunks of 16 bytes, four
 //     per lane), through its own ring of asynchronous copies: every lane
@@ -143,8 +146,8 @@ __device__ __forceinline__ uint32_t max_key_of(uint32_t mx)
 }
 
 template <int DT>
-__device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, const unsigned long long *perm,
-                                                 int msl, int len, int B, int k, int NS,
+__device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, const int *btab, int msl,
+                                                 int len, int B, int k, int NS,
                                                  unsigned long long *cand, Misc *ms)
 {
     using E = Elem<DT>;
@@ -155,7 +158,7 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
     bool any = false;
     int q = warp, pc = 0;  // the producer cursor's first steps
     for (int st = 0; st < nseed && q < msl; ++st) {
-        const int lo = (int)(uint32_t)perm[q] * B;
+        const int lo = btab[q] * B;
         const int nbytes = (min(lo + B, len) - lo) * E::kSize;
         const int nch = (nbytes + 15) >> 4;
         const int c0 = pc * kStageChunks;
@@ -205,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
 
     unsigned char *ring = smem;
     unsigned long long *cand = reinterpret_cast<unsigned long long *>(smem + p.off_cand);
-    unsigned long long *perm = reinterpret_cast<unsigned long long *>(smem + p.off_perm);
+    int *btab = reinterpret_cast<int *>(smem + p.off_perm);  // block at each position
     uint32_t *whist = reinterpret_cast<uint32_t *>(smem + p.off_hist);
     uint16_t *holes = reinterpret_cast<uint16_t *>(smem + p.off_holes);
     Misc *ms = reinterpret_cast<Misc *>(smem + p.off_misc);
@@ -221,28 +224,17 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     const unsigned char *xrow =
         reinterpret_cast<const unsigned char *>(p.x) + (size_t)row * (size_t)p.N * E::kSize;
 
-    // -- random block order: ascending (Philox word 0, block id) -------------
-    const int P = pow2_ceil(msl > 32 ? msl : 32);
-    for (int i = tid; i < P; i += kThreads) {
-        unsigned long long v = ~0ull;
-        if (i < msl) {
-            const uint32_t b = (uint32_t)(first_block + i);
-            const uint32_t w = philox_word0(b, (uint32_t)row, (uint32_t)slice, 0u, p.seed_lo, p.seed_hi);
-            v = ((unsigned long long)w << 32) | b;
-        }
-        perm[i] = v;
+    // -- random block order: a keyed permutation of the slice's blocks (keyed
+    // by Philox from seed, row and slice).  Every warp evaluates the
+    // positions it will scan (w, w+8, ...), one per lane, into a table it
+    // alone reads: no sort and no CTA barrier before the first copies.
+    {
+        BlockOrder order;
+        order.init((uint32_t)msl, philox_word0((uint32_t)row, (uint32_t)slice, 0u, 1u, p.seed_lo, p.seed_hi));
+        for (int q = warp + kWarps * lane; q < msl; q += kWarps * 32)
+            btab[q] = first_block + (int)order((uint32_t)q);
+        __syncwarp();
     }
-    if (tid == 0) {
-        ms->merge_count = 0;
-        ms->pass = 0;
-        ms->check = p.check;
-        ms->ctr[0] = 0;
-        ms->ctr[1] = 0;
-    }
-    __syncthreads();
-    sort_asc_small(perm, msl, P, reinterpret_cast<unsigned long long *>(whist));  // histogram space as scratch
-    for (int i = tid; i < kHistWords; i += kThreads)
-        whist[i] = 0u;  // ordered before the first select by its barriers
 
     const int NS = p.stages;
     unsigned char *wring = ring + (size_t)warp * NS * kStageBytes;
@@ -258,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     const unsigned char *p_src = nullptr;
     auto p_enter = [&]() {
         if (pq < msl) {
-            const int lo = (int)(uint32_t)perm[pq] * B;
+            const int lo = btab[pq] * B;
             p_nbytes = (min(lo + B, len) - lo) * esz;
             p_src = xrow + (size_t)lo * esz + lane * 16;
         }
@@ -291,7 +283,17 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         cp_async_commit();
     };
     for (int s = 0; s < NS - 1; ++s)
-        prefetch(s);
+        prefetch(s);  // the first copies are in flight before the CTA's set-up
+    if (tid == 0) {
+        ms->merge_count = 0;
+        ms->pass = 0;
+        ms->check = p.check;
+        ms->ctr[0] = 0;
+        ms->ctr[1] = 0;
+    }
+    for (int i = tid; i < kHistWords; i += kThreads)
+        whist[i] = 0u;
+    __syncthreads();  // the buffer length words and the histograms are set
 
     int ps = NS - 1;          // slot the next prefetch fills
     int cs = 0;               // slot of the consumer's stage
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     int cq = warp, cpc = 0, c_lo = 0, c_hi = 0, c_nbytes = 0;
     auto c_enter = [&]() {
         if (cq < msl) {
-            c_lo = (int)(uint32_t)perm[cq] * B;
+            c_lo = btab[cq] * B;
             c_hi = min(c_lo + B, len);
             c_nbytes = (c_hi - c_lo) * esz;
         }
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     c_enter();
     Threshold thr = threshold_initial<DT>();
     if (p.k <= kSeedMaxK && msl >= kWarps)
-        thr = seed_threshold<DT>(wring, perm, msl, len, B, p.k, NS, cand, ms);
+        thr = seed_threshold<DT>(wring, btab, msl, len, B, p.k, NS, cand, ms);
 
     while (true) {
         while (cq < msl) {

@@ -184,8 +184,10 @@ long long layout(Plan &pl, int stages, int splits)
     off = align128(off + cap * 8);
     const long long m = (p.N + p.B - 1) / p.B;
     const long long per = (m + splits - 1) / splits;
+    // block order: (Philox word, id) pairs sorted in place (block by block), or
+    // the block id at each position (free-running)
     p.off_perm = (int)off;
-    off = align128(off + (long long)ds::pow2_ceil((int)(per > 32 ? per : 32)) * 8);
+    off = align128(off + (pl.stream ? per * 4 : (long long)ds::pow2_ceil((int)(per > 32 ? per : 32)) * 8));
     p.off_hist = (int)off;
     off = align128(off + ds::kHistWords * 4);
     p.off_holes = (int)off;
