@@ -63,6 +63,7 @@ struct Params {
     int cpw;             // 16-byte chunks per warp of a block
     int cap;             // candidate-buffer entries (free-running scan: overflow bound)
     int identity;        // block-by-block kernel: visit blocks in index order (diagnostic)
+    int pairs;           // free-running kernel: the instance that consumes pieces in pairs (capacity sized for it)
     int off_cand, off_perm, off_hist, off_holes, off_misc;
 };
 

@@ -10,6 +10,9 @@ KernelFn kernel_bf16(bool async, bool wide)
     return wide ? deepselect_topk_kernel<1, false, 16> : deepselect_topk_kernel<1, false, 4>;
 }
 
-KernelFn stream_kernel_bf16() { return deepselect_stream_kernel<1>; }
+KernelFn stream_kernel_bf16(bool pairs)
+{
+    return pairs ? deepselect_stream_kernel<1, true> : deepselect_stream_kernel<1, false>;
+}
 
 }  // namespace ds

@@ -10,6 +10,9 @@ KernelFn kernel_fp16(bool async, bool wide)
     return wide ? deepselect_topk_kernel<2, false, 16> : deepselect_topk_kernel<2, false, 4>;
 }
 
-KernelFn stream_kernel_fp16() { return deepselect_stream_kernel<2>; }
+KernelFn stream_kernel_fp16(bool pairs)
+{
+    return pairs ? deepselect_stream_kernel<2, true> : deepselect_stream_kernel<2, false>;
+}
 
 }  // namespace ds

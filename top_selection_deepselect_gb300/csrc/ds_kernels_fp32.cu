@@ -10,6 +10,9 @@ KernelFn kernel_fp32(bool async, bool wide)
     return wide ? deepselect_topk_kernel<0, false, 16> : deepselect_topk_kernel<0, false, 4>;
 }
 
-KernelFn stream_kernel_fp32() { return deepselect_stream_kernel<0>; }
+KernelFn stream_kernel_fp32(bool pairs)
+{
+    return pairs ? deepselect_stream_kernel<0, true> : deepselect_stream_kernel<0, false>;
+}
 
 }  // namespace ds

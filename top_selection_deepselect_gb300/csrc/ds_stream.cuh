@@ -26,9 +26,11 @@
 //     CTA compacts (radix select) if the buffer reached k + B2, and the
 //     warps go on with the new T.  A reservation that runs past the capacity
 //     fills its slots below the capacity with the composite 0, which is
-//     below every element (no key is 0), and its stage is filtered again
-//     after the compaction.  The capacity is k + B2 + one stage, so at least
-//     k + B2 real entries precede any such filler.
+//     below every element (no key is 0), and its pieces are filtered again
+//     after the compaction.  The capacity is k + B2 + the largest
+//     reservation (one piece, or a pair of pieces when pairs are on), so at
+//     least k + B2 real entries precede any such filler, and the first
+//     reservation after a compaction (at k) always fits.
 // The epilogue (final select, order, or the split-row merge through the
 // cluster) is the block-by-block kernel's.
 #pragma once
@@ -41,6 +43,7 @@ constexpr int kStageChunks = 128;                 // 16-byte chunks of one warp 
 constexpr int kStageBytes = kStageChunks * 16;    // 2 KiB
 constexpr int kLaneChunks = kStageChunks / 32;    // chunks per lane and stage
 constexpr int kMaxStreamStages = 6;               // deepest per-warp ring
+constexpr int kPairChunks = 2 * kStageChunks;      // chunks one reservation covers (two pieces)
 
 __device__ __forceinline__ int ld_volatile_shared(const int *p)
 {
@@ -194,7 +197,7 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
 
 // grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.  Needs
 // 16-byte aligned rows and blocks (the planner checks).
-template <int DT>
+template <int DT, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Params p)
 {
     allow_dependent_grid();
@@ -313,86 +316,149 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     if (p.k <= kSeedMaxK && msl >= kWarps)
         thr = seed_threshold<DT>(wring, btab, msl, len, B, p.k, NS, cand, ms);
 
+    // The partial last chunk of a row is loaded by the lane that filters it.
+    auto load_tail = [&](unsigned char *sp, const BlockView &bv, int nbytes) {
+        const int nch = (nbytes + 15) >> 4;
+        if ((nbytes & 15) && nch - 1 < bv.c1 && ((nch - 1 - bv.c0) & 31) == lane) {
+            const int c = nch - 1;
+            unsigned char *dst = sp + (c - bv.c0) * 16;
+            for (int e = 0; e < kB; ++e) {
+                const int j = bv.lo + c * kB + e;
+                if (j < bv.hi) {
+                    if (DT == 0)
+                        reinterpret_cast<uint32_t *>(dst)[e] = reinterpret_cast<const uint32_t *>(xrow)[j];
+                    else
+                        reinterpret_cast<uint16_t *>(dst)[e] = reinterpret_cast<const uint16_t *>(xrow)[j];
+                }
+            }
+        }
+    };
+
     while (true) {
+        // For small k (seeded threshold, few survivors) pieces are consumed in
+        // pairs (A = the cursor's piece, B = the next one of the walk): both
+        // are folded in one trip, one vote covers them, and their survivors
+        // share one reservation.  With a ring of NS >= 3 pieces, one refill
+        // goes out before the pair is waited for and one after it is
+        // consumed, so NS - 2 pieces stay in flight.  Otherwise B is empty
+        // and a trip consumes one piece.
         while (cq < msl) {
-            const int b0 = cpc * kStageBytes;
-            // prefilter operand for the block's index range (see Threshold)
-            const bool ge = (uint32_t)c_lo < thr.ti;
+            const int b0A = cpc * kStageBytes;
+            int qB = cq, pcB = cpc + 1, loB = c_lo, hiB = c_hi, nbB = c_nbytes;
+            if (b0A + kStageBytes >= c_nbytes) {
+                qB = cq + kWarps;
+                pcB = 0;
+                if (qB < msl) {
+                    loB = btab[qB] * B;
+                    hiB = min(loB + B, len);
+                    nbB = (hiB - loB) * esz;
+                }
+            }
+            const bool hasB = PAIRS && NS >= 3 && qB < msl;
+            const int csB = cs + 1 == NS ? 0 : cs + 1;
             if (!pending) {
                 if (ld_volatile_shared(&ms->ctr[epoch & 1]) >= trigger)
                     break;  // a compaction is due
                 prefetch(ps);
                 ps = ps + 1 == NS ? 0 : ps + 1;
-                cp_async_wait_pending(NS - 1);  // this lane's copies of the stage landed
+                if (hasB)
+                    cp_async_wait_pending(NS - 2);  // this lane's copies of A and B landed
+                else
+                    cp_async_wait_pending(NS - 1);  // this lane's copies of A landed
             }
-            unsigned char *sp = wring + cs * kStageBytes;
-            BlockView bv;
-            bv.lo = c_lo;
-            bv.hi = c_hi;
-            bv.c0 = cpc * kStageChunks;
-            bv.t = ge ? thr.t_ge : thr.t_gt;
-            bv.refine = ge ? (thr.nan_ge || (uint32_t)c_hi > thr.ti) : thr.nan_gt;
-            bv.slot = nullptr;
-            uint32_t mword = 0u;
-            bool any;
-            if (b0 + kStageBytes <= c_nbytes && !bv.refine) {
-                // a whole stage (every chunk copied, no partial chunk) whose
-                // survivors need no per-element check: one maximum per lane
-                const unsigned char *lp = sp + lane * 16;
-                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512);
-                const uint4 v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
+            // prefilter operands per piece, for the block's index range (see Threshold)
+            const bool geA = (uint32_t)c_lo < thr.ti, geB = (uint32_t)loB < thr.ti;
+            BlockView bvA, bvB;
+            bvA.lo = c_lo;
+            bvA.hi = c_hi;
+            bvA.c0 = cpc * kStageChunks;
+            bvA.t = geA ? thr.t_ge : thr.t_gt;
+            bvA.refine = geA ? (thr.nan_ge || (uint32_t)c_hi > thr.ti) : thr.nan_gt;
+            bvA.slot = nullptr;
+            bvB.lo = loB;
+            bvB.hi = hiB;
+            bvB.c0 = pcB * kStageChunks;
+            bvB.t = geB ? thr.t_ge : thr.t_gt;
+            bvB.refine = geB ? (thr.nan_ge || (uint32_t)hiB > thr.ti) : thr.nan_gt;
+            bvB.slot = nullptr;
+            const bool fastA = !bvA.refine && b0A + kStageBytes <= c_nbytes;
+            const bool fastB = hasB && !bvB.refine && (pcB + 1) * kStageBytes <= nbB;
+            unsigned char *spA = wring + cs * kStageBytes;
+            unsigned char *spB = wring + csB * kStageBytes;
+            uint32_t mA = 0u, mB = 0u;
+            // whole pieces clear of T's index: four 16-byte loads at fixed
+            // offsets, one maximum per lane, exact bits for passing lanes
+            if (fastA) {
+                const unsigned char *lp = spA + lane * 16;
+                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512), v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
                 const uint32_t mx = max_nan<DT>(max_nan<DT>(chunk_max<DT>(v0), chunk_max<DT>(v1)),
                                                 max_nan<DT>(chunk_max<DT>(v2), chunk_max<DT>(v3)));
-                const bool pass = max_passes<DT>(mx, bv.t);
-                any = __any_sync(kFull, pass);
-                if (pass)
-                    mword = prefilter_bits<DT>(v0, bv.t) | (prefilter_bits<DT>(v1, bv.t) << kB) |
-                            (prefilter_bits<DT>(v2, bv.t) << (2 * kB)) |
-                            (prefilter_bits<DT>(v3, bv.t) << (3 * kB));
-            } else {
-                // the last stage of a row's last block, or a block that
-                // straddles T's index: chunk bounds and per-element checks
-                const int nch = (c_nbytes + 15) >> 4;
-                bv.c1 = min(bv.c0 + kStageChunks, nch);
-                // the partial last chunk of a row is loaded by the lane that filters it
-                if (!pending && (c_nbytes & 15) && nch - 1 < bv.c1 && ((nch - 1 - bv.c0) & 31) == lane) {
-                    const int c = nch - 1;
-                    unsigned char *dst = sp + (c - bv.c0) * 16;
-                    for (int e = 0; e < kB; ++e) {
-                        const int j = bv.lo + c * kB + e;
-                        if (j < bv.hi) {
-                            if (DT == 0)
-                                reinterpret_cast<uint32_t *>(dst)[e] = reinterpret_cast<const uint32_t *>(xrow)[j];
-                            else
-                                reinterpret_cast<uint16_t *>(dst)[e] = reinterpret_cast<const uint16_t *>(xrow)[j];
-                        }
-                    }
-                }
-                const int slo = bv.lo + bv.c0 * kB;
-                const int shi = min(bv.lo + bv.c1 * kB, bv.hi);
-                bv.plain = !bv.refine && shi - slo == (bv.c1 - bv.c0) * kB;
-                mword = stage_filter<DT>(sp, bv, thr, lane);
-                any = __any_sync(kFull, mword != 0u);
+                if (max_passes<DT>(mx, bvA.t))
+                    mA = prefilter_bits<DT>(v0, bvA.t) | (prefilter_bits<DT>(v1, bvA.t) << kB) |
+                         (prefilter_bits<DT>(v2, bvA.t) << (2 * kB)) | (prefilter_bits<DT>(v3, bvA.t) << (3 * kB));
             }
-            if (any) {
-                const int cnt = (int)__reduce_add_sync(kFull, (uint32_t)__popc(mword));
+            if (fastB) {
+                const unsigned char *lp = spB + lane * 16;
+                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512), v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
+                const uint32_t mx = max_nan<DT>(max_nan<DT>(chunk_max<DT>(v0), chunk_max<DT>(v1)),
+                                                max_nan<DT>(chunk_max<DT>(v2), chunk_max<DT>(v3)));
+                if (max_passes<DT>(mx, bvB.t))
+                    mB = prefilter_bits<DT>(v0, bvB.t) | (prefilter_bits<DT>(v1, bvB.t) << kB) |
+                         (prefilter_bits<DT>(v2, bvB.t) << (2 * kB)) | (prefilter_bits<DT>(v3, bvB.t) << (3 * kB));
+            }
+            // other pieces (a row's partial last piece, a block that
+            // straddles T's index, a NaN operand): chunk bounds and
+            // per-element checks
+            if (!fastA) {
+                bvA.c1 = min(bvA.c0 + kStageChunks, (c_nbytes + 15) >> 4);
+                if (!pending)
+                    load_tail(spA, bvA, c_nbytes);
+                const int slo = bvA.lo + bvA.c0 * kB, shi = min(bvA.lo + bvA.c1 * kB, bvA.hi);
+                bvA.plain = !bvA.refine && shi - slo == (bvA.c1 - bvA.c0) * kB;
+                mA = stage_filter<DT>(spA, bvA, thr, lane);
+            }
+            if (hasB && !fastB) {
+                bvB.c1 = min(bvB.c0 + kStageChunks, (nbB + 15) >> 4);
+                if (!pending)
+                    load_tail(spB, bvB, nbB);
+                const int slo = bvB.lo + bvB.c0 * kB, shi = min(bvB.lo + bvB.c1 * kB, bvB.hi);
+                bvB.plain = !bvB.refine && shi - slo == (bvB.c1 - bvB.c0) * kB;
+                mB = stage_filter<DT>(spB, bvB, thr, lane);
+            }
+            if (__any_sync(kFull, (mA | mB) != 0u)) {
+                // one reservation for both pieces: the two warp counts in
+                // one sum (16-bit halves; a piece has at most 1024 elements)
+                const uint32_t both = __reduce_add_sync(kFull, (uint32_t)__popc(mA) | ((uint32_t)__popc(mB) << 16));
+                const int cntA = (int)(both & 0xFFFFu), cnt = cntA + (int)(both >> 16);
                 int base = 0;
                 if (lane == 0)
                     base = atomicAdd(&ms->ctr[epoch & 1], cnt);
                 base = __shfl_sync(kFull, base, 0);
                 if (base + cnt > cap) {
                     // no room: fill what lies below the capacity with the
-                    // composite 0 and filter this stage again after the
+                    // composite 0 and filter both pieces again after the
                     // compaction
                     for (int i = base + lane; i < cap; i += 32)
                         cand[i] = 0ull;
                     pending = true;
                     break;
                 }
-                stage_append<DT>(sp, bv, lane, mword, cand + base);
+                if (cntA)
+                    stage_append<DT>(spA, bvA, lane, mA, cand + base);
+                if (cnt > cntA)
+                    stage_append<DT>(spB, bvB, lane, mB, cand + base + cntA);
             }
             pending = false;
-            if (b0 + kStageBytes >= c_nbytes) {
+            if (hasB) {
+                // past B; then refill A's slot (its loads are done)
+                cq = qB;
+                cpc = pcB;
+                c_lo = loB;
+                c_hi = hiB;
+                c_nbytes = nbB;
+                cs = csB;
+            }
+            if ((cpc + 1) * kStageBytes >= c_nbytes) {
                 cq += kWarps;
                 cpc = 0;
                 c_enter();
@@ -400,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                 ++cpc;
             }
             cs = cs + 1 == NS ? 0 : cs + 1;
+            if (hasB) {
+                prefetch(ps);
+                ps = ps + 1 == NS ? 0 : ps + 1;
+            }
         }
 
         // -- sync point: all eight warps ------------------------------------
@@ -430,9 +500,10 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                      row, slice, xrow, 0, 0, 0, 0);
 }
 
-// Free-running kernel entry points of one dtype, defined in ds_kernels_<dtype>.cu.
-KernelFn stream_kernel_fp32();
-KernelFn stream_kernel_bf16();
-KernelFn stream_kernel_fp16();
+// Free-running kernel entry points of one dtype (pairs of pieces or single
+// pieces), defined in ds_kernels_<dtype>.cu.
+KernelFn stream_kernel_fp32(bool pairs);
+KernelFn stream_kernel_bf16(bool pairs);
+KernelFn stream_kernel_fp16(bool pairs);
 
 }  // namespace ds

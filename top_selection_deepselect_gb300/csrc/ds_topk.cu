@@ -94,25 +94,26 @@ int device_info(DevInfo **out, int *dev_out)
 
 using ds::KernelFn;
 
-// 15 instantiations: the block-by-block kernel per dtype x asynchronous
+// 18 instantiations: the block-by-block kernel per dtype x asynchronous
 // copies x mask rounds (4 rounds cover blocks of up to 2 KiB per warp, 16 up
-// to 8 KiB per warp), and the free-running kernel per dtype.
-KernelFn kernel_for(int dtype, bool stream, bool async, bool wide, int *slot)
+// to 8 KiB per warp), and the free-running kernel per dtype x pairs.
+KernelFn kernel_for(int dtype, bool stream, bool pairs, bool async, bool wide, int *slot)
 {
     if (stream) {
-        *slot = 12 + dtype;
-        return dtype == DS_FP32 ? ds::stream_kernel_fp32()
-             : dtype == DS_BF16 ? ds::stream_kernel_bf16() : ds::stream_kernel_fp16();
+        *slot = 12 + dtype * 2 + (pairs ? 1 : 0);
+        return dtype == DS_FP32 ? ds::stream_kernel_fp32(pairs)
+             : dtype == DS_BF16 ? ds::stream_kernel_bf16(pairs) : ds::stream_kernel_fp16(pairs);
     }
     *slot = dtype * 4 + (async ? 2 : 0) + (wide ? 1 : 0);
     return dtype == DS_FP32 ? ds::kernel_fp32(async, wide)
          : dtype == DS_BF16 ? ds::kernel_bf16(async, wide) : ds::kernel_fp16(async, wide);
 }
 
-int ensure_attributes(DevInfo &d, int dtype, bool stream, bool async, bool wide, KernelFn *fn)
+int ensure_attributes(DevInfo &d, int dtype, bool stream, bool pairs, bool async, bool wide,
+                      KernelFn *fn)
 {
     int slot = 0;
-    *fn = kernel_for(dtype, stream, async, wide, &slot);
+    *fn = kernel_for(dtype, stream, pairs, async, wide, &slot);
     std::lock_guard<std::mutex> lock(g_mu);
     if (d.attr_set & (1u << slot))
         return DS_OK;
@@ -171,9 +172,16 @@ long long layout(Plan &pl, int stages, int splits)
     const long long ring_merge = splits > 1 ? (long long)splits * p.k * 8 : 0;
     long long off = align128(ring_stream > ring_merge ? ring_stream : ring_merge);
     // block by block: k + B + B2 (the largest length the loop reaches);
-    // free-running: k + B2 + one stage's elements (reservations beyond
-    // that are filled with the composite 0 and retried after a compaction)
-    long long cap = pl.stream ? (long long)p.k + p.B2 + (long long)ds::kStageChunks * pl.per_chunk
+    // free-running: k + B2 + the largest reservation, a pair of pieces
+    // (reservations beyond that are filled with the composite 0 and retried
+    // after a compaction; the first reservation after a compaction starts
+    // at k and always fits, so every retry makes progress)
+    // pairs only where the first threshold is seeded (small k): from -inf a
+    // pair reserves two whole pieces, and the larger buffer makes the first
+    // select larger (DSA index scores, k = 512: 27.7 -> 38.9 us with pairs)
+    p.pairs = pl.stream && p.k <= ds::kSeedMaxK ? 1 : 0;
+    long long cap = pl.stream ? (long long)p.k + p.B2 +
+                                    (long long)(p.pairs ? ds::kPairChunks : ds::kStageChunks) * pl.per_chunk
                               : (long long)p.k + p.B + p.B2;
     if (cap < ds::pow2_ceil(p.k))
         cap = ds::pow2_ceil(p.k);
@@ -410,7 +418,8 @@ int launch(const void *x, int dtype, int rows, const int32_t *row_len, int64_t N
     if ((rc = make_plan(x, dtype, rows, N, k, B, B2, splits_req, stats != nullptr, *d, pl)) != DS_OK)
         return rc;
     KernelFn fn = nullptr;
-    if ((rc = ensure_attributes(*d, dtype, pl.stream, pl.async, pl.p.cpw > 128, &fn)) != DS_OK)
+    if ((rc = ensure_attributes(*d, dtype, pl.stream, pl.p.pairs != 0, pl.async, pl.p.cpw > 128, &fn)) !=
+        DS_OK)
         return rc;
     // a cluster must fit on one GPC: shrink an automatic split factor until
     // the hardware can hold at least one cluster
