@@ -64,6 +64,7 @@ struct Params {
     int cap;             // candidate-buffer entries (free-running scan: overflow bound)
     int identity;        // block-by-block kernel: visit blocks in index order (diagnostic)
     int pairs;           // free-running kernel: the instance that consumes pieces in pairs (capacity sized for it)
+    int hist_words;      // histogram region: 3 x 256 words, or kHistWords when a select can exceed 6144 entries
     int off_cand, off_perm, off_hist, off_holes, off_misc;
 };
 
@@ -876,7 +877,7 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_topk_kernel(const Para
     }
     __syncthreads();
     sort_asc_small(perm, msl, P, reinterpret_cast<unsigned long long *>(whist));  // histogram space as scratch
-    for (int i = tid; i < kHistWords; i += kThreads)
+    for (int i = tid; i < p.hist_words; i += kThreads)
         whist[i] = 0u;  // ordered before the first select by its barriers
 
     const int bps = p.bps;

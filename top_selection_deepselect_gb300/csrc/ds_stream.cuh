@@ -201,7 +201,12 @@ template <int DT, bool PAIRS>
 __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Params p)
 {
     allow_dependent_grid();
-    dependent_grid_wait();  // before the first read of x, row_len or the outputs
+    // Rows of full length: everything up to the first copies (block order,
+    // shared-memory set-up) reads no input, so it runs before waiting for
+    // the previous grid on the stream; with row_len the wait comes first.
+    const bool wait_late = p.row_len == nullptr;
+    if (!wait_late)
+        dependent_grid_wait();
     using E = Elem<DT>;
     constexpr int kB = E::kPerChunk;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -285,8 +290,6 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         }
         cp_async_commit();
     };
-    for (int s = 0; s < NS - 1; ++s)
-        prefetch(s);  // the first copies are in flight before the CTA's set-up
     if (tid == 0) {
         ms->merge_count = 0;
         ms->pass = 0;
@@ -294,8 +297,12 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
         ms->ctr[0] = 0;
         ms->ctr[1] = 0;
     }
-    for (int i = tid; i < kHistWords; i += kThreads)
+    for (int i = tid; i < p.hist_words; i += kThreads)
         whist[i] = 0u;
+    if (wait_late)
+        dependent_grid_wait();  // before the first read of x or the outputs
+    for (int s = 0; s < NS - 1; ++s)
+        prefetch(s);  // each warp's first copies go out before the CTA barrier
     __syncthreads();  // the buffer length words and the histograms are set
 
     int ps = NS - 1;          // slot the next prefetch fills

@@ -196,8 +196,15 @@ long long layout(Plan &pl, int stages, int splits)
     // the block id at each position (free-running)
     p.off_perm = (int)off;
     off = align128(off + (pl.stream ? per * 4 : (long long)ds::pow2_ceil((int)(per > 32 ? per : 32)) * 8));
+    // digit histograms: three rotating 256-bin buffers for the register
+    // select; the per-warp histograms of the shared-memory select only when
+    // a select can exceed the register select's 6144 entries (the buffer, or
+    // the union of a split row in CTA 0)
+    const long long reg_max = 24LL * ds::kThreads;
+    const bool big_select = cap > reg_max || (splits > 1 && (long long)splits * p.k > reg_max);
+    p.hist_words = big_select ? ds::kHistWords : 3 * ds::kHistBins;
     p.off_hist = (int)off;
-    off = align128(off + ds::kHistWords * 4);
+    off = align128(off + (long long)p.hist_words * 4);
     p.off_holes = (int)off;
     off = align128(off + (long long)p.k * 2);
     p.off_misc = (int)off;
