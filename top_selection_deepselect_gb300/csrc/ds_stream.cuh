@@ -195,6 +195,56 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
     return tkey == 0u ? threshold_initial<DT>() : threshold_from<DT>((unsigned long long)tkey << 32);
 }
 
+// The survivors of a pair of pieces in one loop: bits 0..31 of `m` are
+// piece A's (as stage_filter numbers them), bits 32..63 piece B's.  Every
+// round each lane with survivors left writes its next one at the slot after
+// those of the lower lanes; the number of rounds is the largest count of a
+// lane, known before the loop.
+template <int DT>
+__device__ __forceinline__ void pair_append(const unsigned char *spA, const BlockView &bvA,
+                                            const unsigned char *spB, const BlockView &bvB, int lane,
+                                            unsigned long long m, unsigned long long *dst)
+{
+    using E = Elem<DT>;
+    constexpr int kB = E::kPerChunk;
+    const int rounds = (int)__reduce_max_sync(kFull, (uint32_t)__popcll(m));
+    int run = 0;
+    for (int r = 0; r < rounds; ++r) {
+        const bool has = m != 0ull;
+        const uint32_t b = __ballot_sync(kFull, has);
+        if (has) {
+            const int bit = __ffsll((long long)m) - 1;
+            m &= m - 1ull;
+            const bool inB = bit >= 32;
+            const int i = (bit & 31) / kB, e = (bit & 31) % kB;
+            const unsigned char *ep = (inB ? spB : spA) + (lane + 32 * i) * 16 + e * E::kSize;
+            const uint32_t bits = DT == 0 ? *reinterpret_cast<const uint32_t *>(ep)
+                                          : (uint32_t)*reinterpret_cast<const uint16_t *>(ep);
+            const int lo = inB ? bvB.lo : bvA.lo, c0 = inB ? bvB.c0 : bvA.c0;
+            const uint32_t idx = (uint32_t)(lo + (c0 + lane + 32 * i) * kB + e);
+            dst[run + __popc(b & lanemask_lt(lane))] =
+                ((unsigned long long)E::key(bits) << 32) | (unsigned long long)(~idx);
+        }
+        run += __popc(b);
+    }
+}
+
+// Exact survivor bits of one whole piece held in registers (4 chunks per
+// lane): bits only for the chunks whose own maximum passes (small k, where
+// survivors are sparse).
+template <int DT>
+__device__ __forceinline__ uint32_t whole_piece_bits(const uint4 (&v)[kLaneChunks], const uint32_t (&cm)[kLaneChunks],
+                                                     uint32_t t)
+{
+    constexpr int kB = Elem<DT>::kPerChunk;
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < kLaneChunks; ++i)
+        if (max_passes<DT>(cm[i], t))
+            m |= prefilter_bits<DT>(v[i], t) << (i * kB);
+    return m;
+}
+
 // grid = rows * splits, cluster = (splits, 1, 1) when splits > 1.  Needs
 // 16-byte aligned rows and blocks (the planner checks).
 template <int DT, bool PAIRS>
@@ -397,21 +447,24 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
             // offsets, one maximum per lane, exact bits for passing lanes
             if (fastA) {
                 const unsigned char *lp = spA + lane * 16;
-                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512), v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
-                const uint32_t mx = max_nan<DT>(max_nan<DT>(chunk_max<DT>(v0), chunk_max<DT>(v1)),
-                                                max_nan<DT>(chunk_max<DT>(v2), chunk_max<DT>(v3)));
+                const uint4 v[kLaneChunks] = {lds128(lp), lds128(lp + 512), lds128(lp + 1024), lds128(lp + 1536)};
+                const uint32_t cm[kLaneChunks] = {chunk_max<DT>(v[0]), chunk_max<DT>(v[1]), chunk_max<DT>(v[2]),
+                                                  chunk_max<DT>(v[3])};
+                const uint32_t mx = max_nan<DT>(max_nan<DT>(cm[0], cm[1]), max_nan<DT>(cm[2], cm[3]));
                 if (max_passes<DT>(mx, bvA.t))
-                    mA = prefilter_bits<DT>(v0, bvA.t) | (prefilter_bits<DT>(v1, bvA.t) << kB) |
-                         (prefilter_bits<DT>(v2, bvA.t) << (2 * kB)) | (prefilter_bits<DT>(v3, bvA.t) << (3 * kB));
+                    mA = PAIRS ? whole_piece_bits<DT>(v, cm, bvA.t)
+                               : prefilter_bits<DT>(v[0], bvA.t) | (prefilter_bits<DT>(v[1], bvA.t) << kB) |
+                                     (prefilter_bits<DT>(v[2], bvA.t) << (2 * kB)) |
+                                     (prefilter_bits<DT>(v[3], bvA.t) << (3 * kB));
             }
             if (fastB) {
                 const unsigned char *lp = spB + lane * 16;
-                const uint4 v0 = lds128(lp), v1 = lds128(lp + 512), v2 = lds128(lp + 1024), v3 = lds128(lp + 1536);
-                const uint32_t mx = max_nan<DT>(max_nan<DT>(chunk_max<DT>(v0), chunk_max<DT>(v1)),
-                                                max_nan<DT>(chunk_max<DT>(v2), chunk_max<DT>(v3)));
+                const uint4 v[kLaneChunks] = {lds128(lp), lds128(lp + 512), lds128(lp + 1024), lds128(lp + 1536)};
+                const uint32_t cm[kLaneChunks] = {chunk_max<DT>(v[0]), chunk_max<DT>(v[1]), chunk_max<DT>(v[2]),
+                                                  chunk_max<DT>(v[3])};
+                const uint32_t mx = max_nan<DT>(max_nan<DT>(cm[0], cm[1]), max_nan<DT>(cm[2], cm[3]));
                 if (max_passes<DT>(mx, bvB.t))
-                    mB = prefilter_bits<DT>(v0, bvB.t) | (prefilter_bits<DT>(v1, bvB.t) << kB) |
-                         (prefilter_bits<DT>(v2, bvB.t) << (2 * kB)) | (prefilter_bits<DT>(v3, bvB.t) << (3 * kB));
+                    mB = whole_piece_bits<DT>(v, cm, bvB.t);
             }
             // other pieces (a row's partial last piece, a block that
             // straddles T's index, a NaN operand): chunk bounds and
@@ -433,10 +486,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                 mB = stage_filter<DT>(spB, bvB, thr, lane);
             }
             if (__any_sync(kFull, (mA | mB) != 0u)) {
-                // one reservation for both pieces: the two warp counts in
-                // one sum (16-bit halves; a piece has at most 1024 elements)
-                const uint32_t both = __reduce_add_sync(kFull, (uint32_t)__popc(mA) | ((uint32_t)__popc(mB) << 16));
-                const int cntA = (int)(both & 0xFFFFu), cnt = cntA + (int)(both >> 16);
+                // one reservation for both pieces
+                const int cnt = (int)__reduce_add_sync(kFull, (uint32_t)(__popc(mA) + __popc(mB)));
                 int base = 0;
                 if (lane == 0)
                     base = atomicAdd(&ms->ctr[epoch & 1], cnt);
@@ -450,10 +501,11 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
                     pending = true;
                     break;
                 }
-                if (cntA)
+                if (PAIRS)  // few survivors: one loop over both pieces
+                    pair_append<DT>(spA, bvA, spB, bvB, lane,
+                                    (unsigned long long)mA | ((unsigned long long)mB << 32), cand + base);
+                else        // dense pieces at the start of a large-k scan
                     stage_append<DT>(spA, bvA, lane, mA, cand + base);
-                if (cnt > cntA)
-                    stage_append<DT>(spB, bvB, lane, mB, cand + base + cntA);
             }
             pending = false;
             if (hasB) {
