@@ -134,31 +134,84 @@ def profile_traffic(workload, kernel):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples taken by a background thread while
-    the GPU works: one complete query per call (no streamed output that a
-    terminated child could leave unflushed), every ~50 ms."""
+    """Clock / throttle samples taken by a background thread while the GPU
+    works, every ~50 ms: read-only NVML queries in this process (ctypes on
+    libnvidia-ml), or one complete nvidia-smi query per sample if NVML
+    cannot be loaded."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40}
 
     def __init__(self, index):
-        self.index = index
-        self.rows = []
+        self.index = int(index)
+        self.samples = []  # (sm_mhz, max_mhz, reason names)
         self.thread = None
         self.stop_flag = False
+        self.error = None
+        self.nvml = None
+        self.handle = None
 
-    def _query(self):
+    def _nvml_open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            rc = lib.nvmlInit_v2()
+            if rc != 0:
+                self.error = "nvmlInit_v2 returned %d" % rc
+                return False
+            h = ctypes.c_void_p()
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h))
+            if rc != 0:
+                self.error = "nvmlDeviceGetHandleByIndex_v2 returned %d" % rc
+                return False
+            self.nvml, self.handle = lib, h
+            return True
+        except Exception as ex:  # no NVML here: fall back to nvidia-smi
+            self.error = "nvml: %r" % (ex,)
+            return False
+
+    def _nvml_sample(self):
+        import ctypes
+        sm, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(sm)) != 0:  # NVML_CLOCK_SM
+            return None
+        if self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) != 0:
+            return None
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        reasons = set()
+        if fn(self.handle, ctypes.byref(rs)) == 0:
+            reasons = {n for n, b in self.REASON_BITS.items() if rs.value & b}
+        return float(sm.value), float(mx.value), reasons
+
+    def _smi_sample(self):
+        # a library path that points at the toolkit's driver stubs would make
+        # nvidia-smi load a stub NVML, so the child gets a clean one
+        env = {k: v for k, v in os.environ.items() if k not in ("LD_LIBRARY_PATH", "LD_PRELOAD")}
+        out = ""
         try:
             r = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
                                 "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                               timeout=10)
-            return [l.strip().split(", ") for l in r.stdout.splitlines() if l.strip()]
-        except Exception:
-            return []
+                               timeout=10, env=env)
+            out = r.stdout.strip()
+            f = out.split(", ")
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            return (float(f[1]), float(f[2]),
+                    {n for n, v in zip(names, f[5:9]) if v.strip() == "Active"})
+        except Exception as ex:  # recorded, not fatal
+            if "nvidia-smi" not in (self.error or ""):
+                self.error = (self.error + "; " if self.error else "") + "nvidia-smi: %s" % (out[:80] or repr(ex))
+            return None
 
     def _loop(self):
+        use_nvml = self._nvml_open()
         while not self.stop_flag:
-            self.rows.extend(self._query())
+            smp = self._nvml_sample() if use_nvml else self._smi_sample()
+            if smp is not None:
+                self.samples.append(smp)
             time.sleep(0.05)
 
     def start(self):
@@ -166,33 +219,27 @@ class ClockSampler:
         self.thread = threading.Thread(target=self._loop, daemon=True)
         self.thread.start()
         t0 = time.perf_counter()
-        while not self.rows and time.perf_counter() - t0 < 5.0:  # the sampler is running
+        while not self.samples and time.perf_counter() - t0 < 5.0:  # the sampler is running
             time.sleep(0.02)
 
     def stop(self):
         if self.thread is None:
             return None
-        n_before = len(self.rows)
+        n_before = len(self.samples)
         t0 = time.perf_counter()
-        while len(self.rows) == n_before and time.perf_counter() - t0 < 2.0:
+        while len(self.samples) == n_before and time.perf_counter() - t0 < 2.0:
             time.sleep(0.02)  # at least one sample after the timed steps were enqueued
         self.stop_flag = True
         self.thread.join(timeout=15)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in self.rows:
-            try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                for name, v in zip(names, r[5:9]):
-                    if v.strip() == "Active":
-                        reasons.add(name)
-            except (IndexError, ValueError):
-                continue
-        if not sm:
-            return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"error": self.error or "no clock samples"}
+        sm = [x[0] for x in self.samples]
+        reasons = set()
+        for x in self.samples:
+            reasons |= x[2]
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(x[1] for x in self.samples),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 def rank_rows(rank, world, rows, scaling):
@@ -656,8 +703,8 @@ def run_ours(args, rank, world):
         r0, r1, batch_rows = rank_rows(rank, world, rows, args.scaling)
         # weak: this rank's slice of the batch is a full copy of the workload's
         # rows; strong: it is the rows [r0, r1) of the workload itself
-        local = (0, rows) if args.scaling == "weak" else (r0, r1)
-        wl = Workload(args.workload, dev, torch, ds, l2, local_rows=local)
+        span = (0, rows) if args.scaling == "weak" else (r0, r1)
+        wl = Workload(args.workload, dev, torch, ds, l2, local_rows=span)
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
