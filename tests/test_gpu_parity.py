@@ -188,6 +188,24 @@ def test_ties_and_special_values(dtype, kind):
 
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
+@pytest.mark.parametrize("kind", ["normal", "specials", "levels", "constant", "ascending"])
+def test_first_threshold_for_large_k(dtype, kind):
+    # k above 128 starts from a threshold taken from the chunk maxima of each
+    # warp's first stages (one range histogram): k on both sides of every
+    # group count (1, 2, 4, 8, 16 groups per lane), small blocks that leave
+    # lanes without chunks, ragged rows around k + B2, ties at the bin edge
+    bits, _ = workloads.generate(6, 40000, dtype, kind, seed=43, fraction=0.3, value=0.5)
+    row_len = np.array([40000, 39999, 5000, 3000, 1200, 20000], dtype=np.int32)
+    for k, B, B2, splits in [(129, 1024, 64, 1), (256, 64, 64, 1), (257, 512, 256, 0),
+                             (512, 1024, 128, 1), (513, 64, 512, 2), (1024, 1024, 256, 1),
+                             (1025, 256, 1024, 3), (2048, 1024, 64, 1), (2049, 512, 512, 1),
+                             (4096, 1024, 1024, 1)]:
+        ref_idx, ref_val = oracle.topk(bits, dtype, k, row_len=row_len)
+        idx, val = run(bits, dtype, k, B, B2, row_len=row_len, splits=splits)
+        assert_same(idx, val, ref_idx, ref_val)
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("kind", ["normal", "specials", "levels", "ascending"])
 def test_split_rows_with_a_large_union(dtype, kind):
     # splits * k above 8192: every slice sorts its own top k and CTA 0 merges
@@ -435,8 +453,9 @@ def test_plans_of_the_workloads():
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         assert plan["grid"] <= sms * plan["ctas_per_sm"]
         if sms == 152:
-            # short rows: one CTA per SM; long rows: two per SM
-            want = {"small_fp32": 16, "dsa_index_bf16": 2, "sampling_logits_bf16": 1,
-                    "adversarial_fp32": 8}
+            # rows under 128 KiB stay whole (slices keep 64 KiB); long rows
+            # fill two CTAs per SM
+            want = {"small_fp32": 1, "dsa_index_bf16": 1, "dsa_decode_ragged_fp32": 8,
+                    "sampling_logits_bf16": 1, "adversarial_fp32": 8}
             if name in want:
                 assert s == want[name], (name, plan)

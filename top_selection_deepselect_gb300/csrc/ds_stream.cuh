@@ -195,6 +195,132 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
     return tkey == 0u ? threshold_initial<DT>() : threshold_from<DT>((unsigned long long)tkey << 32);
 }
 
+// The first threshold for larger k (kSeedMaxK < k <= kSeedMaxWideK).  256
+// lane maxima are too few, so the maxima of single 16-byte chunks are used
+// (four per lane and stage, each a different element of the row), and T is
+// not their exact k-th but the lower edge of the histogram bin that holds
+// it: any key with k chunk maxima at or above it has k elements at or above
+// it.  One pass of 256 bins spans [kmin, kmax] of the maxima, where kmin is
+// already a lower bound on their k-th largest: each lane's chunk slots are
+// cut into G >= k/256 groups (by chunk position; for G = 8 also by stage
+// parity; G = 16: every slot), and the smallest of a lane's G group maxima
+// has G maxima of that lane at or above it, so the minimum of these over
+// the lanes has 256G >= k maxima above it.  Lanes with an empty group drop
+// out of that minimum; when fewer than k/G lanes remain, kmin is the
+// smallest maximum.  With fewer than k maxima in all, T stays -inf.
+constexpr int kSeedMaxWideK = 16 * kThreads;
+static_assert(kHistBins == kThreads, "one histogram bin per thread");
+
+template <int DT>
+__device__ __noinline__ Threshold seed_threshold_wide(const unsigned char *wring, const int *btab, int msl,
+                                                      int len, int B, int k, int NS, uint32_t *hist,
+                                                      Misc *ms)
+{
+    using E = Elem<DT>;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nseed = kSeedStages < NS - 1 ? kSeedStages : NS - 1;
+    cp_async_wait_pending(NS - 1 - nseed);  // this lane's copies of its first nseed stages landed
+    uint32_t ck[4][kLaneChunks];  // chunk maximum keys by stage and slot; 0: no chunk
+    int q = warp, pc = 0;
+#pragma unroll
+    for (int st = 0; st < 4; ++st) {
+        const bool have = st < nseed && q < msl;
+        int nbytes = 0, c0 = 0;
+        if (have) {
+            const int lo = btab[q] * B;
+            nbytes = (min(lo + B, len) - lo) * E::kSize;
+            c0 = pc * kStageChunks;
+        }
+#pragma unroll
+        for (int i = 0; i < kLaneChunks; ++i) {
+            const int c = c0 + lane + 32 * i;
+            ck[st][i] = (have && (c + 1) * 16 <= nbytes)
+                            ? max_key_of<DT>(chunk_max<DT>(lds128(wring + st * kStageBytes + (lane + 32 * i) * 16)))
+                            : 0u;
+        }
+        if (have) {
+            if (c0 + kStageChunks >= ((nbytes + 15) >> 4)) {
+                q += kWarps;
+                pc = 0;
+            } else {
+                ++pc;
+            }
+        }
+    }
+    const int G = k <= kThreads ? 1 : k <= 2 * kThreads ? 2 : k <= 4 * kThreads ? 4
+                                    : k <= 8 * kThreads ? 8 : 16;
+    uint32_t gp[2][kLaneChunks], gi[kLaneChunks];
+    uint32_t vmin = 0xFFFFFFFFu, nvalid = 0u, all_min = 0xFFFFFFFFu;
+#pragma unroll
+    for (int i = 0; i < kLaneChunks; ++i) {
+        gp[0][i] = max(ck[0][i], ck[2][i]);
+        gp[1][i] = max(ck[1][i], ck[3][i]);
+        gi[i] = max(gp[0][i], gp[1][i]);
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+            vmin = ck[st][i] ? min(vmin, ck[st][i]) : vmin;
+            nvalid += ck[st][i] ? 1u : 0u;
+            all_min = min(all_min, ck[st][i]);
+        }
+    }
+    const uint32_t vmax = max(max(gi[0], gi[1]), max(gi[2], gi[3]));
+    uint32_t bound;  // the smallest of this lane's G group maxima (0: a group is empty)
+    if (G == 1)
+        bound = vmax;
+    else if (G == 2)
+        bound = min(max(gi[0], gi[2]), max(gi[1], gi[3]));
+    else if (G == 4)
+        bound = min(min(gi[0], gi[1]), min(gi[2], gi[3]));
+    else if (G == 8)
+        bound = min(min(min(gp[0][0], gp[0][1]), min(gp[0][2], gp[0][3])),
+                    min(min(gp[1][0], gp[1][1]), min(gp[1][2], gp[1][3])));
+    else
+        bound = all_min;
+    const uint32_t wmax = __reduce_max_sync(kFull, vmax);
+    const uint32_t wbound = __reduce_min_sync(kFull, bound ? bound : 0xFFFFFFFFu);
+    const uint32_t wlanes = (uint32_t)__popc(__ballot_sync(kFull, bound != 0u));
+    const uint32_t wvmin = __reduce_min_sync(kFull, vmin);
+    const uint32_t wvalid = __reduce_add_sync(kFull, nvalid);
+    if (lane == 0) {
+        ms->wor[warp] = ((unsigned long long)wmax << 32) | wbound;
+        ms->wand[warp] = ((unsigned long long)wvmin << 32) | wlanes;
+        ms->wsum[warp] = wvalid;
+    }
+    __syncthreads();
+    uint32_t kmax = 0u, kbound = 0xFFFFFFFFu, kvmin = 0xFFFFFFFFu, lanes = 0u, valid = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const unsigned long long a = ms->wor[w], b = ms->wand[w];
+        kmax = max(kmax, (uint32_t)(a >> 32));
+        kbound = min(kbound, (uint32_t)a);
+        kvmin = min(kvmin, (uint32_t)(b >> 32));
+        lanes += (uint32_t)b;
+        valid += ms->wsum[w];
+    }
+    uint32_t kmin;
+    if (lanes * (uint32_t)G >= (uint32_t)k)
+        kmin = kbound;
+    else if (valid >= (uint32_t)k)
+        kmin = kvmin;
+    else
+        return threshold_initial<DT>();  // the same decision in every thread
+    const uint32_t span = kmax - kmin;
+    const int sh = span >= 256u ? (32 - __clz(span)) - 8 : 0;  // (span >> sh) < 256
+#pragma unroll
+    for (int st = 0; st < 4; ++st)
+#pragma unroll
+        for (int i = 0; i < kLaneChunks; ++i)
+            if (ck[st][i] >= kmin)
+                atomicAdd(&hist[(ck[st][i] - kmin) >> sh], 1u);
+    __syncthreads();
+    if (warp == 0)
+        digit_search(hist, (uint32_t)k, lane, ms);  // at least k maxima are counted
+    __syncthreads();
+    const uint32_t tkey = kmin + (ms->sel_digit << sh);
+    hist[tid] = 0u;  // the histogram is left zero (one bin per thread)
+    return threshold_from<DT>((unsigned long long)tkey << 32);
+}
+
 // The survivors of a pair of pieces in one loop: bits 0..31 of `m` are
 // piece A's (as stage_filter numbers them), bits 32..63 piece B's.  Every
 // round each lane with survivors left writes its next one at the slot after
@@ -372,6 +498,8 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     Threshold thr = threshold_initial<DT>();
     if (p.k <= kSeedMaxK && msl >= kWarps)
         thr = seed_threshold<DT>(wring, btab, msl, len, B, p.k, NS, cand, ms);
+    else if (p.k <= kSeedMaxWideK && msl >= kWarps && (long long)msl * B >= (long long)trigger)
+        thr = seed_threshold_wide<DT>(wring, btab, msl, len, B, p.k, NS, whist, ms);
 
     // The partial last chunk of a row is loaded by the lane that filters it.
     auto load_tail = [&](unsigned char *sp, const BlockView &bv, int nbytes) {

@@ -215,6 +215,7 @@ long long layout(Plan &pl, int stages, int splits)
 constexpr long long kMaxPermBlocks = 4096;  // blocks per slice the in-CTA order holds
 constexpr long long kMaxAutoSplits = 16;     // largest automatic split factor
 constexpr long long kStreamSliceBytes = 128 * 1024;  // slices that keep a second CTA per SM busy
+constexpr long long kMinSliceBytes = 64 * 1024;      // free-running kernel: smallest automatic slice
 
 int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B2, int splits_req,
               bool stats, DevInfo &d, Plan &pl)
@@ -288,6 +289,11 @@ int make_plan(const void *x, int dtype, int rows, int64_t N, int k, int B, int B
             two /= 2;
         const long long slice_bytes = (m + two - 1) / two * (long long)B * esz;
         splits = (int)(two > one && slice_bytes >= kStreamSliceBytes ? two : one);
+        // the free-running kernel's first threshold leaves short slices with
+        // few or no compactions, and then the cluster merge costs more than
+        // the parallel scan saves: its slices keep kMinSliceBytes at least
+        while (pl.stream && splits > 1 && (m + splits - 1) / splits * (long long)B * esz < kMinSliceBytes)
+            splits /= 2;
     }
     if (splits > 1 && (long long)splits * k * 8 > budget_one)
         return fail(DS_EUNSUPPORTED, "splits * k * 8 = %lld bytes does not fit shared memory",
