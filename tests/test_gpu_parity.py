@@ -208,13 +208,14 @@ def test_first_threshold_for_large_k(dtype, kind):
 @pytest.mark.parametrize("dtype", ["fp32", "bf16", "fp16"])
 @pytest.mark.parametrize("kind", ["normal", "specials", "levels", "ascending"])
 def test_split_rows_with_a_large_union(dtype, kind):
-    # splits * k above 8192: every slice sorts its own top k and CTA 0 merges
-    # the sorted runs pairwise (odd split counts carry a run to the next
-    # round); ragged rows leave some slices short or empty
+    # splits * k above 8192: one radix select over the union of the slices'
+    # candidates, its histograms summed across the cluster, then CTA 0
+    # orders the k selected entries; ragged rows leave some slices short or
+    # empty, odd split counts included
     bits, _ = workloads.generate(6, 60000, dtype, kind, seed=29, fraction=0.2, value=0.0)
     row_len = np.array([60000, 0, 1500, 4095, 33333, 59999], dtype=np.int32)
     for k, B, B2, splits in [(1100, 512, 512, 8), (1300, 1024, 256, 7), (2000, 512, 1024, 5),
-                             (4096, 1024, 1024, 3)]:
+                             (4096, 1024, 1024, 3), (5000, 1024, 1024, 2)]:
         ref_idx, ref_val = oracle.topk(bits, dtype, k, row_len=row_len)
         idx, val = run(bits, dtype, k, B, B2, row_len=row_len, splits=splits)
         assert_same(idx, val, ref_idx, ref_val)
@@ -222,13 +223,14 @@ def test_split_rows_with_a_large_union(dtype, kind):
 
 @pytest.mark.parametrize("dtype", ["fp32", "bf16"])
 @pytest.mark.parametrize("kind", ["normal", "constant", "levels", "specials", "ascending"])
-def test_split_rows_pruned_by_the_largest_slice_threshold(dtype, kind):
-    # 6144 < splits * k <= 8192: slices send CTA 0 only entries at or above
-    # the largest slice k-th composite (ties across slices, short and empty
-    # slices included)
+def test_split_rows_select_across_the_cluster_or_pruned(dtype, kind):
+    # 6144 < splits * k <= 8192: the select across the cluster; k above
+    # 6144: slices send CTA 0 only entries at or above the largest slice
+    # k-th composite (ties across slices, short and empty slices included)
     bits, _ = workloads.generate(5, 50000, dtype, kind, seed=37, fraction=0.2, value=-1.5)
     row_len = np.array([50000, 0, 900, 7000, 49999], dtype=np.int32)
-    for k, B, B2, splits in [(900, 512, 512, 7), (1024, 1024, 512, 8), (1600, 256, 1024, 4)]:
+    for k, B, B2, splits in [(900, 512, 512, 7), (1024, 1024, 512, 8), (1600, 256, 1024, 4),
+                             (6500, 512, 512, 2)]:
         ref_idx, ref_val = oracle.topk(bits, dtype, k, row_len=row_len)
         idx, val = run(bits, dtype, k, B, B2, row_len=row_len, splits=splits)
         assert_same(idx, val, ref_idx, ref_val)

@@ -575,16 +575,19 @@ struct Misc {
     int merge_count;                     // CTA 0 of a cluster: entries received
     int merge_off;                       // this CTA's offset in CTA 0's merge buffer
     unsigned int *check;                 // bounds-checked builds: violation bits (null otherwise)
-    int runlen[16];                      // CTA 0 of a cluster: length of each slice's sorted run
     unsigned long long tslice[16];       // split rows: every slice's k-th composite (0: fewer than k)
     int pass;                            // select: digit passes so far (histogram rotation)
     int ctr[2];                          // free-running scan: buffer length, one word per epoch
     __align__(16) int rem[kWarps];       // free-running scan: warp still has stages (at a sync point)
+    unsigned long long cl_or, cl_and;    // split rows: OR / AND of this slice's candidates
+    int cl_n, cl_cnt;                    // split rows: this slice's candidates / entries selected
 };
 
 // Digit histograms: the register select uses one 256-bin histogram of 32-bit
-// counters per CTA, three rotating buffers; the shared-memory select uses one
-// per warp.  Both leave the region zero.
+// counters per CTA, three rotating buffers; each pass clears the buffer of
+// the next, so the buffer a call starts with (ms->pass mod 3) is clear, while
+// up to two others may be left dirty.  The shared-memory select uses one
+// histogram per warp over the whole region and clears it on entry.
 constexpr int kHistBins = 256;
 constexpr int kHistWords = kWarps * kHistBins;  // 8 KiB
 static_assert(3 * kHistBins <= kHistWords, "rotating buffers fit the region");

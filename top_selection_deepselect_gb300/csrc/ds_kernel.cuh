@@ -333,13 +333,15 @@ __device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, cons
             emit<DT>(p, obase, ranks[j], vals[j], xrow);
 }
 
-// Largest k for which CTA 0 merges the slices' sorted runs (every thread
-// holds at most kMergeOut outputs of a merge round in registers).
+// Outputs a thread holds in registers in one round of a merge-path sort.
 constexpr int kMergeOut = 16;
-constexpr int kMergeMaxK = kThreads * kMergeOut;
-// Below this many entries in the union, CTA 0 selects from the union
-// directly (registers hold it) instead of merging sorted runs.
-constexpr int kMergeMinUnion = 8192;
+// Split rows whose union of slice results (splits * k) exceeds
+// kClusterSelectMinUnion take the select across the cluster when k is at
+// most kClusterSelectMaxK (a slice's entries fit the register select after
+// its own select at most); smaller unions go to CTA 0 whole, and unions of
+// larger k go there pruned.
+constexpr int kClusterSelectMaxK = 24 * kThreads;
+constexpr int kClusterSelectMinUnion = 24 * kThreads;
 
 // Outputs [t0, t1) (at most kMergeOut) of the descending merge of runs A[0, la)
 // and B[0, lb): a merge-path search finds how many of the first t0 come from
@@ -596,120 +598,210 @@ __device__ __forceinline__ void sort_and_write(unsigned long long *arr, int cnt,
 // rank computations as sort_and_write; every entry moves to its rank).  arr
 // holds pow2_ceil(cnt) entries.  Caller synchronises before; ends
 // synchronised.
-template <int E>
-__device__ __forceinline__ void sort_runs_inplace(unsigned long long *arr, int cnt)
-{
-    for (int i = cnt + threadIdx.x; i < 256 * E; i += kThreads)
-        arr[i] = 0ull;
-    __syncthreads();
-    unsigned long long vals[E];
-    int ranks[E];
-    rank_desc_runs<E>(arr, vals, ranks);
-#pragma unroll
-    for (int j = 0; j < E; ++j)
-        if (vals[j] != 0ull)
-            arr[ranks[j]] = vals[j];
-    __syncthreads();
-}
+// ---------------------------------------------------------------------------
+// The top k of a split row by one RadixSelectTopK ("算法", step 3) over the
+// union of the slices' candidates, taken across the cluster: no slice
+// selects, sorts or ships its own top k first.  Each pass every CTA counts
+// its live entries into its own 256-bin histogram; after a cluster barrier
+// every CTA sums the S histograms through distributed shared memory, so all
+// of them see the same counts and take the same digit decisions (warp 0's
+// digit search, as in radix_select_regs).  The passes go on until every
+// entry of the chosen digit is needed; the composites are distinct, so the
+// selected entries (higher digits, plus that digit) are exactly the k
+// largest of the union.  Each CTA then copies its selected entries into
+// CTA 0's buffer `dst0` after those of the lower slices.  Histograms rotate
+// over three buffers (cleared on entry), and a buffer is cleared again one
+// cluster barrier after the pass whose sums read it; the sums go to a fourth
+// 256-word buffer, and all four are left zero.  All
+// threads of all CTAs of the cluster call it (every CTA passes the same
+// cluster barriers); it returns the number of entries in dst0, which is
+// min(k, size of the union), and ends with CTA 0's copy complete.
+// ---------------------------------------------------------------------------
+static_assert(4 * kHistBins <= kHistWords, "the cluster select uses four histogram buffers");
 
-static __device__ __noinline__ void sort_desc_inplace(unsigned long long *arr, int cnt)
+template <int R>
+static __device__ __noinline__ int cluster_select(const unsigned long long *cand, int n, int k, int S,
+                                                  unsigned long long *dst0, int dst_room,
+                                                  uint32_t *whist, Misc *ms)
 {
-    if (cnt <= kThreads) {
-        const int t = threadIdx.x;
-        unsigned long long e = 0ull;
-        int rank = 0;
-        if (t < cnt) {
-            e = arr[t];
-            for (int j = 0; j < cnt; ++j)
-                rank += arr[j] > e ? 1 : 0;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int slice = (int)cluster.block_rank();
+    uint32_t hi[R], lo[R], dg[R];
+    uint32_t valid = 0u;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int i = tid + kThreads * j;
+        hi[j] = 0u;
+        lo[j] = 0u;
+        dg[j] = 0u;
+        if (i < n) {
+            const unsigned long long c = cand[i];
+            hi[j] = (uint32_t)(c >> 32);
+            lo[j] = (uint32_t)c;
+            valid |= 1u << j;
         }
-        __syncthreads();
-        if (t < cnt)
-            arr[rank] = e;
-        __syncthreads();
-    } else if (cnt <= 512) {
-        sort_runs_inplace<2>(arr, cnt);
-    } else if (cnt <= 1024) {
-        sort_runs_inplace<4>(arr, cnt);
-    } else if (cnt <= 2048) {
-        merge_sort_desc<0, false>(arr, cnt, 0, Out{nullptr, nullptr, 0}, 0, nullptr);
-    } else {
-        const int P = pow2_ceil(cnt);
-        for (int i = cnt + threadIdx.x; i < P; i += kThreads)
-            arr[i] = 0ull;
-        __syncthreads();
-        bitonic_sort_smem(arr, P, true);
     }
-}
-
-// CTA 0 of a split row: runs[s*k, s*k + ms->runlen[s]) holds slice s's top k
-// sorted descending.  Runs are merged pairwise, keeping the first k of each
-// merge (stride 1, 2, 4, ...: run s absorbs run s + stride), in place: each
-// round's outputs are held in registers across a barrier.  The last merge
-// writes the row's output directly.  Called by all threads of CTA 0.
-template <int DT>
-__device__ __forceinline__ void merge_runs_and_write(unsigned long long *runs, int S, const Out &p,
-                                                  int row, const unsigned char *xrow, Misc *ms)
-{
-    using E = Elem<DT>;
-    const int k = p.k, tid = threadIdx.x;
-    const long long obase = (long long)row * k;
-    for (int st = 1; st < S; st <<= 1) {
-        const bool last = 2 * st >= S;  // one pair left: (0, st)
-        int np = 0;                     // pairs (s, s + st), s = 2 st m, s + st < S
-        for (int s = 0; s + st < S; s += 2 * st)
-            ++np;
-        int G = 1;  // pairs per group: a power of two, at most kMergeOut outputs per thread
-        while (2 * G <= np && 2 * G * k <= kMergeMaxK)
-            G *= 2;
-        const int tpp = kThreads / G;
-        for (int g0 = 0; g0 < np; g0 += G) {
-            const int pair = g0 + tid / tpp, local = tid % tpp;
-            unsigned long long out[kMergeOut];
-            int s = 0, t0 = 0, t1 = 0, L = 0;
-            if (pair < np) {
-                s = pair * 2 * st;
-                const int la = ms->runlen[s], lb = ms->runlen[s + st];
-                L = la + lb < k ? la + lb : k;
-                const int chunk = (L + tpp - 1) / tpp;
-                t0 = local * chunk < L ? local * chunk : L;
-                t1 = t0 + chunk < L ? t0 + chunk : L;
-                if (t0 < t1)
-                    merge_chunk(runs + (size_t)s * k, la, runs + (size_t)(s + st) * k, lb, t0, t1, out);
-            }
-            if (last) {
+    // bits that vary over the union, and its size
+    uint32_t oh = 0u, ol = 0u, ah = ~0u, al = ~0u;
 #pragma unroll
-                for (int q = 0; q < kMergeOut; ++q)
-                    if (q < t1 - t0)
-                        emit<DT>(p, obase, t0 + q, out[q], xrow);
-                for (int i = L + tid; i < k; i += kThreads) {
-                    p.idx[obase + i] = -1;
-                    if (DT == 0)
-                        reinterpret_cast<uint32_t *>(p.val)[obase + i] = E::kNegInfBits;
-                    else
-                        reinterpret_cast<uint16_t *>(p.val)[obase + i] = (uint16_t)E::kNegInfBits;
-                }
-                return;
-            }
-            __syncthreads();  // every read of this group's runs is done
+    for (int j = 0; j < R; ++j) {
+        if (valid & (1u << j)) {
+            oh |= hi[j];
+            ol |= lo[j];
+            ah &= hi[j];
+            al &= lo[j];
+        }
+    }
+    oh = __reduce_or_sync(kFull, oh);
+    ol = __reduce_or_sync(kFull, ol);
+    ah = __reduce_and_sync(kFull, ah);
+    al = __reduce_and_sync(kFull, al);
+    if (lane == 0) {
+        ms->wor[warp] = ((unsigned long long)oh << 32) | ol;
+        ms->wand[warp] = ((unsigned long long)ah << 32) | al;
+    }
+    // the selects of the scan leave two of their three rotating buffers
+    // dirty: clear all four here (nothing reads them remotely yet)
 #pragma unroll
-            for (int q = 0; q < kMergeOut; ++q)
-                if (q < t1 - t0)
-                    runs[(size_t)s * k + t0 + q] = out[q];
-            if (pair < np && local == 0)
-                ms->runlen[s] = L;
+    for (int b = 0; b < 4; ++b)
+        whist[b * kHistBins + tid] = 0u;
+    __syncthreads();
+    if (tid == 0) {
+        unsigned long long vo = 0ull, va = ~0ull;
+        for (int w = 0; w < kWarps; ++w) {
+            vo |= ms->wor[w];
+            va &= ms->wand[w];
+        }
+        ms->cl_or = vo;
+        ms->cl_and = va;
+        ms->cl_n = n;
+    }
+    cluster.sync();  // every slice's summary is published; the buffers are clear
+    unsigned long long go = 0ull, ga = ~0ull;
+    long long tot = 0;
+    for (int s = 0; s < S; ++s) {
+        const Misc *pm = cluster.map_shared_rank(ms, s);
+        go |= pm->cl_or;  // an empty slice has OR 0 and AND all ones
+        ga &= pm->cl_and;
+        tot += pm->cl_n;
+    }
+    uint32_t sel = valid;
+    int last = -1;  // histogram buffer of the last pass
+    uint32_t *sums = whist + 3 * kHistBins;
+    if (tot > k) {
+        const unsigned long long vary = go ^ ga;  // nonzero: at least two distinct entries
+        uint32_t need = (uint32_t)k, live = valid, above = 0u;
+        int h = 63 - __clzll((long long)vary);
+        int pass = 0;
+        while (true) {
+            const int sh = h >= 7 ? h - 7 : 0;
+            uint32_t *cur = whist + (pass % 3) * kHistBins;
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                const uint32_t d = (sh >= 32 ? hi[j] >> (sh - 32) : __funnelshift_r(lo[j], hi[j], sh)) & 255u;
+                dg[j] = d;
+                if (live & (1u << j))
+                    atomicAdd(&cur[d], 1u);
+            }
+            cluster.sync();  // every slice's counts of this pass are in
+            if (pass >= 1)
+                whist[((pass - 1) % 3) * kHistBins + tid] = 0u;  // every slice summed it before the barrier
+            uint32_t g = 0u;
+            for (int s = 0; s < S; ++s)
+                g += cluster.map_shared_rank(cur, s)[tid];
+            sums[tid] = g;
             __syncthreads();
+            if (warp == 0)
+                digit_search(sums, need, lane, ms);
+            __syncthreads();
+            const uint32_t dsel = ms->sel_digit, eq = ms->sel_eq;
+            need -= ms->sel_above;
+            last = pass % 3;
+            ++pass;
+#pragma unroll
+            for (int j = 0; j < R; ++j) {
+                if (live & (1u << j)) {
+                    if (dg[j] > dsel)
+                        above |= 1u << j;
+                    if (dg[j] != dsel)
+                        live &= ~(1u << j);
+                }
+            }
+            if (eq == need)
+                break;
+            const unsigned long long below = sh > 0 ? (vary & ((1ull << sh) - 1ull)) : 0ull;
+            if (below == 0ull)
+                break;  // unreachable for distinct composites; keeps the loop finite
+            h = 63 - __clzll((long long)below);
         }
+        sel = above | live;
     }
+    // this slice's selected entries go to CTA 0 after the lower slices' ones
+    const int mine = warp_count<R>(sel);
+    if (lane == 0)
+        ms->wsum[warp] = (uint32_t)mine;
+    __syncthreads();
+    int wbase = 0, cnt = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        wbase += w < warp ? (int)ms->wsum[w] : 0;
+        cnt += (int)ms->wsum[w];
+    }
+    if (tid == 0)
+        ms->cl_cnt = cnt;
+    cluster.sync();  // counts published; every slice has summed the last histograms
+    if (last >= 0)
+        whist[last * kHistBins + tid] = 0u;
+    sums[tid] = 0u;
+    int base = 0, total = 0;
+    for (int s = 0; s < S; ++s) {
+        const int c = cluster.map_shared_rank(ms, s)->cl_cnt;
+        base += s < slice ? c : 0;
+        total += c;
+    }
+    if (DS_GUARD(ms, base + cnt <= dst_room, 64u))
+        warp_scatter<R>(sel, hi, lo, cluster.map_shared_rank(dst0, 0) + base + wbase, lane);
+    cluster.sync();  // CTA 0 holds the selected entries
+    return total;
+}
+
+// A split row with a large union: the row's top k by one select across
+// the cluster into CTA 0's ring (free once every CTA has finished
+// streaming, which the select's first cluster barrier ensures), then CTA 0
+// orders it.  cnt = this slice's entries in cand.  A function of its own:
+// kept out of finish_slice, it leaves the scan loop's register allocation
+// as it was (measured: the stream kernel's stack frame and the sampling
+// logits' time).
+template <int DT>
+static __device__ __noinline__ void finish_by_cluster(const Out o, unsigned char *ring, unsigned long long *cand,
+                                                      uint32_t *whist, Misc *ms, int cnt, int S, int row,
+                                                      int slice, const unsigned char *xrow)
+{
+    unsigned long long *dst = reinterpret_cast<unsigned long long *>(ring);
+    const int droom = (int)(cand - dst);
+    int total;
+    if (cnt <= 4 * kThreads)
+        total = cluster_select<4>(cand, cnt, o.k, S, dst, droom, whist, ms);
+    else if (cnt <= 8 * kThreads)
+        total = cluster_select<8>(cand, cnt, o.k, S, dst, droom, whist, ms);
+    else if (cnt <= 12 * kThreads)
+        total = cluster_select<12>(cand, cnt, o.k, S, dst, droom, whist, ms);
+    else
+        total = cluster_select<24>(cand, cnt, o.k, S, dst, droom, whist, ms);
+    if (slice == 0)
+        sort_and_write<DT>(dst, total < o.k ? total : o.k, o, row, xrow, whist, ms, droom);
 }
 
 // ---------------------------------------------------------------------------
 // Epilogue of one slice: final TopK, counters, then the ordered output (one
 // CTA per row) or the cluster merge (split rows).  A separate function so
 // that the streaming loop is compiled on its own.  Called by all threads
-// after the scan; the candidate buffer holds n entries.
+// after the scan; the candidate buffer holds n entries.  WIDE = false
+// leaves out the select across the cluster, for callers whose splits * k
+// never exceeds kClusterSelectMinUnion.
 // ---------------------------------------------------------------------------
-template <int DT>
+template <int DT, bool WIDE = true>
 static __device__ __noinline__ void finish_slice(const Out o, long long *stats, unsigned char *ring,
                                                  unsigned long long *cand, int room, uint32_t *whist,
                                                  uint16_t *holes, Misc *ms, int n, int S, int row,
@@ -721,10 +813,15 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
     // one CTA per row with at most one entry per thread: ranking the entries
     // selects and orders them at once (sort_and_write)
     const bool rank_all = S == 1 && n <= kThreads;
+    // a split row with a large union: one select over the whole cluster,
+    // which takes a slice's candidates as they are when they fit registers
+    const bool by_cluster =
+        WIDE && S > 1 && o.k <= kClusterSelectMaxK && (long long)S * o.k > kClusterSelectMinUnion;
+    const bool whole = by_cluster && n <= 24 * kThreads;
     unsigned long long tk = 0ull;  // this slice's k-th composite (0: fewer than k entries)
-    if (n > o.k && !rank_all)
+    if (n > o.k && !rank_all && !whole)
         tk = select_topk(cand, n, o.k, room, whist, holes, ms);
-    const int cnt = rank_all ? n : (n < o.k ? n : o.k);
+    const int cnt = rank_all || whole ? n : (n < o.k ? n : o.k);
     if (stats != nullptr && tid == 0) {
         long long *s = stats + ((long long)row * S + slice) * 4;
         s[0] = A;
@@ -740,22 +837,8 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
 
     // -- split rows: partial top-k of every slice into CTA 0 -------------------
     cg::cluster_group cluster = cg::this_cluster();
-    if (o.k <= kMergeMaxK && (long long)S * o.k > kMergeMinUnion) {
-        // a large union: each slice sorts its own top k, CTA 0 merges the
-        // sorted runs (cheaper than selecting from S*k entries in shared
-        // memory)
-        sort_desc_inplace(cand, cnt);
-        cluster.sync();  // every CTA has finished streaming; CTA 0's ring is free
-        unsigned long long *dst =
-            cluster.map_shared_rank(reinterpret_cast<unsigned long long *>(ring), 0) + (size_t)slice * o.k;
-        if (DS_GUARD(ms, (long long)slice * o.k + cnt <= cand - reinterpret_cast<unsigned long long *>(ring), 8u))
-            for (int i = tid; i < cnt; i += kThreads)
-                dst[i] = cand[i];
-        if (tid == 0)
-            *cluster.map_shared_rank(&ms->runlen[slice], 0) = cnt;
-        cluster.sync();
-        if (slice == 0)
-            merge_runs_and_write<DT>(reinterpret_cast<unsigned long long *>(ring), S, o, row, xrow, ms);
+    if (by_cluster) {
+        finish_by_cluster<DT>(o, ring, cand, whist, ms, cnt, S, row, slice, xrow);
         return;
     }
     // otherwise CTA 0 selects the top k of the union and orders it.  For a

@@ -209,6 +209,8 @@ __device__ __noinline__ Threshold seed_threshold(const unsigned char *wring, con
 // out of that minimum; when fewer than k/G lanes remain, kmin is the
 // smallest maximum.  With fewer than k maxima in all, T stays -inf.
 constexpr int kSeedMaxWideK = 16 * kThreads;
+static_assert((long long)kMaxSplits * kSeedMaxK <= kClusterSelectMinUnion,
+              "the pairs instance (k <= kSeedMaxK) never needs the select across the cluster");
 static_assert(kHistBins == kThreads, "one histogram bin per thread");
 
 template <int DT>
@@ -683,8 +685,10 @@ __global__ void __launch_bounds__(kThreads, 2) deepselect_stream_kernel(const Pa
     const int n = ms->ctr[epoch & 1];
     __syncthreads();  // every thread read the length; this thread's copies have landed
 
-    finish_slice<DT>(Out{p.out_idx, p.out_val, p.k}, nullptr, ring, cand, cap, whist, holes, ms, n, S,
-                     row, slice, xrow, 0, 0, 0, 0);
+    // with pairs (k <= 128) a union of slices holds at most 16 * 128 entries,
+    // so that instance leaves out the select across the cluster
+    finish_slice<DT, !PAIRS>(Out{p.out_idx, p.out_val, p.k}, nullptr, ring, cand, cap, whist, holes, ms,
+                             n, S, row, slice, xrow, 0, 0, 0, 0);
 }
 
 // Free-running kernel entry points of one dtype (pairs of pieces or single

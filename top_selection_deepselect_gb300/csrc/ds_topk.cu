@@ -199,7 +199,8 @@ long long layout(Plan &pl, int stages, int splits)
     // digit histograms: three rotating 256-bin buffers for the register
     // select; the per-warp histograms of the shared-memory select only when
     // a select can exceed the register select's 6144 entries (the buffer, or
-    // the union of a split row in CTA 0)
+    // the union of a split row in CTA 0).  The cluster select of a split row
+    // (splits * k above 8192) uses four 256-bin buffers of that region.
     const long long reg_max = 24LL * ds::kThreads;
     const bool big_select = cap > reg_max || (splits > 1 && (long long)splits * p.k > reg_max);
     p.hist_words = big_select ? ds::kHistWords : 3 * ds::kHistBins;
