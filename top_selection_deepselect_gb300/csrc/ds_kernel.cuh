@@ -329,7 +329,7 @@ __device__ __forceinline__ void emit_runs(unsigned long long *arr, int cnt, cons
     rank_desc_runs<E>(arr, vals, ranks);
 #pragma unroll
     for (int j = 0; j < E; ++j)
-        if (vals[j] != 0ull)
+        if (vals[j] != 0ull && ranks[j] < p.k)
             emit<DT>(p, obase, ranks[j], vals[j], xrow);
 }
 
@@ -810,9 +810,10 @@ static __device__ __noinline__ void finish_slice(const Out o, long long *stats, 
 {
     const int tid = threadIdx.x;
     W += n;
-    // one CTA per row with at most one entry per thread: ranking the entries
-    // selects and orders them at once (sort_and_write)
-    const bool rank_all = S == 1 && n <= kThreads;
+    // one CTA per row with at most 1024 entries: ordering them all and
+    // writing the first k selects them too (sort_and_write), cheaper than a
+    // select followed by the order of k (DSA index scores: 552 entries, k = 512)
+    const bool rank_all = S == 1 && (n <= kThreads || (n <= 4 * kThreads && room >= 4 * kThreads));
     // a split row with a large union: one select over the whole cluster,
     // which takes a slice's candidates as they are when they fit registers
     const bool by_cluster =
