@@ -100,9 +100,11 @@ int ds_topk(const void *x, int dtype, int rows, const int32_t *row_len, int64_t 
  *   splits   0: automatic; 1: one CTA per row; 2..16: the m = ceil(len/B)
  *            blocks of a row are cut into `splits` contiguous slices of
  *            ceil(m/splits) blocks, one CTA of a thread-block cluster scans
- *            each slice, and the top k of the slices' union is selected in
- *            CTA 0 (splits * k <= 6144) or by one radix select across the
- *            cluster (section "实现", last paragraph).  The automatic factor
+ *            each slice, and the top k of the slices' union is selected by
+ *            one radix select across the cluster (splits * k > 6144 and
+ *            k <= 6144) or in CTA 0 (otherwise; for k > 6144 only entries at
+ *            or above the largest slice k-th are sent) (section "实现", last
+ *            paragraph).  The automatic factor
  *            is a power of two that fills the SMs with one CTA each (two when
  *            slices still hold 128 KiB); calls without counters keep slices of
  *            at least 64 KiB.
