@@ -770,9 +770,7 @@ static __device__ __noinline__ int cluster_select(const unsigned long long *cand
 // the cluster into CTA 0's ring (free once every CTA has finished
 // streaming, which the select's first cluster barrier ensures), then CTA 0
 // orders it.  cnt = this slice's entries in cand.  A function of its own:
-// kept out of finish_slice, it leaves the scan loop's register allocation
-// as it was (measured: the stream kernel's stack frame and the sampling
-// logits' time).
+// inside finish_slice it grew the stream kernel's stack frame (ptxas).
 template <int DT>
 static __device__ __noinline__ void finish_by_cluster(const Out o, unsigned char *ring, unsigned long long *cand,
                                                       uint32_t *whist, Misc *ms, int cnt, int S, int row,
